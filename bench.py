@@ -1,0 +1,490 @@
+#!/usr/bin/env python3
+"""Benchmark of branch attention forward + backward on one GB300.
+
+One step = ba_forward + ba_backward over the whole 256K-token EAGLE-3 TTT
+workload (1 sequence of 262144 main tokens, depth 7, 32 q / 8 kv heads,
+head_dim 128, virtual CP degree 8), inputs resident in HBM.  Prints ONE JSON
+line (rank 0).  Under torchrun each rank runs an independent replica (the
+path has no data exchange on one GPU per process: replicas only) and the
+timing is the max over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle instead (host cores, bounded
+sample of the same workload).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "branch-attn fwd+bwd useful TFLOP/s at 256K tokens; % of bf16 tensor peak"
+UNIT = "TFLOP/s"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        top = max(smax)
+        loaded = [x for x in sm if x >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": top, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- oracle sample (CPU)
+
+
+class _HostSource:
+    """Oracle input source prefetched to host memory (rows of the sampled
+    units and the main K/V columns), so that only the oracle is timed."""
+
+    def __init__(self, wl, tensors, units):
+        import oracle
+        self.wl = wl
+        qids = np.concatenate([oracle.keysets.queries_of_unit(wl, u) for u in units])
+        self.qpos = {int(q): i for i, q in enumerate(qids)}
+        self.bpos = self.qpos
+        fetch = lambda name, heads: tensors[name].reshape(-1, heads, wl.head_dim).index_select(
+            0, _idx(qids, tensors[name].device)).float().cpu().double().numpy()
+        self.q = fetch("q_b", wl.heads_q)
+        self.do = fetch("d_o", wl.heads_q)
+        self.kb = fetch("k_b", wl.heads_kv)
+        self.vb = fetch("v_b", wl.heads_kv)
+        self.km = tensors["k_m"].float().cpu().double().numpy()
+        self.vm = tensors["v_m"].float().cpu().double().numpy()
+        self._main = {}
+
+    def rows(self, name, ids):
+        src = {"q_b": self.q, "d_o": self.do, "k_b": self.kb, "v_b": self.vb}[name]
+        return src[[self.qpos[int(i)] for i in ids]]
+
+    def main(self, name, kh):
+        key = (name, kh)
+        if key not in self._main:
+            self._main[key] = np.ascontiguousarray((self.km if name == "k_m" else self.vm)[:, kh])
+        return self._main[key]
+
+
+def _idx(ids, device):
+    import torch
+    return torch.as_tensor(np.asarray(ids, dtype=np.int64), device=device)
+
+
+def _unit_flops(wl, unit):
+    """Useful fwd + bwd flops of every query-head row of one anchor unit."""
+    import oracle
+    qids = oracle.keysets.queries_of_unit(wl, unit)
+    pairs = int(oracle.keysets.key_count(wl, qids).sum()) * wl.heads_q
+    return 4.0 * wl.head_dim * pairs * 3.5
+
+
+def oracle_sample(wl, tensors, budget_s: float, seed: int = 7, max_units: int = 256):
+    """Times the CPU oracle on seeded anchor units until ~budget_s of work.
+    Returns (useful TFLOP/s, units, seconds, threads)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    nu = oracle.keysets.num_units(wl)
+    units = [int(u) for u in rng.choice(nu, size=min(nu, max_units), replace=False)]
+    src = _HostSource(wl, tensors, units)
+    done, flops, t0 = 0, 0.0, time.perf_counter()
+    for u in units:
+        oracle.attention.unit_eval(wl, src, [u], grads=True)
+        done += 1
+        flops += _unit_flops(wl, u)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, done, dt
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------- our arm
+
+
+def kernel_bytes(wl, info, name):
+    """Algorithmic HBM bytes per step of a memory-bound kernel."""
+    R = info["query_rows"]
+    d = wl.head_dim
+    T = wl.tokens
+    nbk = (wl.depth * T if wl.family == "ttt" else wl.num_anchors * wl.block) * wl.heads_kv
+    if name == "zigzag_pack":  # both passes pack q, k_m, v_m, k_b, v_b: read + write
+        return 2 * 2 * 2 * (R * d + 2 * T * wl.heads_kv * d + 2 * nbk * d)
+    if name == "lse_merge":
+        return R * (2 * d * 4 + 2 * 4) + R * (d * 2 + 4)
+    if name == "bwd_prep":
+        return R * (2 * d * 2 + 4) + R * (d * 2 + 2 * 4 + d * 4)
+    if name == "branch_fwd":
+        return R * d * 2 + 2 * nbk * d * 2 + R * (d * 4 + 4)
+    if name == "branch_bwd":
+        return R * (2 * d * 2 + 2 * 4 + d * 4) + 2 * nbk * d * 2 + R * d * 2 + 2 * nbk * d * 2
+    return None
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from branch_attention_speculative_gb300 import api, workloads as W
+
+    peaks = load_peaks()
+    wl = W.config(args.config)
+    plan = api.Plan.from_workload(wl)
+    info = plan.info()
+    t = W.make_tensors(wl, device="cuda")
+    ws = plan.workspace()
+    o = torch.empty_like(t["q_b"])
+    lse = torch.empty(t["q_b"].shape[:-1], dtype=torch.float32, device="cuda")
+    grads = {"dq_b": torch.empty_like(t["q_b"]), "dk_m": torch.empty_like(t["k_m"]),
+             "dv_m": torch.empty_like(t["v_m"]), "dk_b": torch.empty_like(t["k_b"]),
+             "dv_b": torch.empty_like(t["v_b"])}
+
+    def step():
+        plan.forward(t["q_b"], t["k_m"], t["v_m"], t["k_b"], t["v_b"], o=o, lse=lse, workspace=ws)
+        plan.backward(t["q_b"], t["k_m"], t["v_m"], t["k_b"], t["v_b"], o, lse, t["d_o"], grads=grads,
+                      workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = plan.check_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    plan.profile(True)
+    plan.profile_read()
+    sampler = ClockSampler(local)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    barrier(world)
+    clocks = sampler.stop()
+    kt = plan.profile_read()
+    plan.profile(False)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms, world)
+    status = plan.check_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after timed steps")
+
+    flops = info["fwd_flops"] + info["bwd_flops"]
+    value = world * flops / (ms / 1e3) / 1e12
+    peak_t = peaks["bf16_tflops_sustained"]
+
+    kernels = {}
+    for name, (n, tot) in kt.items():
+        per = tot / max(n, 1)
+        ent = {"launches": n, "ms_total_per_step": tot / args.steps, "ms_per_launch": per}
+        if name in ("main_fwd", "main_bwd"):
+            f = 4.0 * wl.head_dim * info["main_pairs"] * (1.0 if name == "main_fwd" else 2.5)
+            ent["achieved"] = f / (tot / args.steps / 1e3) / 1e12
+            ent["unit"] = "TFLOP/s"
+        else:
+            b = kernel_bytes(wl, info, name)
+            if b is not None:
+                ent["achieved"] = b / (tot / args.steps / 1e3) / 1e9
+                ent["unit"] = "GB/s"
+        kernels[name] = ent
+    dom = max(kt.items(), key=lambda kv: kv[1][1])[0] if kt else None
+    roofline = None
+    if dom is not None:
+        e = kernels[dom]
+        if e.get("unit") == "TFLOP/s":
+            roofline = {"kernel": dom, "bound": "tensor", "achieved": e["achieved"], "peak": peak_t,
+                        "unit": "TFLOP/s", "frac": e["achieved"] / peak_t, "traffic": None,
+                        "peak_source": f"bf16_tflops_sustained ({peaks['source']})"}
+        else:
+            roofline = {"kernel": dom, "bound": "hbm", "achieved": e["achieved"], "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": e["achieved"] / peaks["hbm_gbs"], "traffic": None,
+                        "peak_source": f"hbm_gbs ({peaks['source']})"}
+    launches = sum(n for n, _ in kt.values())
+
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(args, plan, wl, t, info, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, units, secs = oracle_sample(wl, t, args.cpu_budget)
+        cpu = {"value": tf, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": f"{units} seeded anchor units (all {wl.steps} steps x {wl.heads_q} heads each, fwd+bwd, "
+                         f"fp64 numpy) of the same workload, {secs:.1f} s"}
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 inputs)",
+        "config": {"workload": wl.name, "family": wl.family, "tokens": wl.tokens, "ttt_depth": wl.depth,
+                   "heads_q": wl.heads_q, "heads_kv": wl.heads_kv, "head_dim": wl.head_dim, "cp_virtual": wl.cp,
+                   "fwd_flops": info["fwd_flops"], "bwd_flops": info["bwd_flops"],
+                   "l2": "inputs larger than L2 (tens of GB per step)", "parallelism": f"replicas x{world}"},
+        "pct_of_bf16_peak": value / world / peak_t,
+        "wall_s_timed": wall1 - wall0,
+        "roofline": roofline,
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def _mem_available_bytes():
+    try:
+        for ln in open("/proc/meminfo"):
+            if ln.startswith("MemAvailable:"):
+                return int(ln.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def run_e2e(args, plan, wl, t, info, world):
+    """Same metric through the public API with host buffers: every step
+    copies its inputs host->device from pinned memory and reads the results
+    back device->host inside the timed region."""
+    import torch
+    ins = ["q_b", "k_m", "v_m", "k_b", "v_b", "d_o"]
+    outs = {"o": t["q_b"], "lse": None, "dq_b": t["q_b"], "dk_m": t["k_m"], "dv_m": t["v_m"], "dk_b": t["k_b"],
+            "dv_b": t["v_b"]}
+    in_bytes = sum(t[n].numel() * t[n].element_size() for n in ins)
+    lse_shape = t["q_b"].shape[:-1]
+    out_bytes = sum(v.numel() * v.element_size() for k, v in outs.items() if v is not None) + \
+        int(np.prod(lse_shape)) * 4
+    need = in_bytes + out_bytes
+    if _mem_available_bytes() < 1.25 * need:
+        return {"value": None, "unit": UNIT, "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+                "skipped": f"host memory available {_mem_available_bytes() / 1e9:.0f} GB < {1.25 * need / 1e9:.0f} GB"}
+    h_in = {n: torch.empty(t[n].shape, dtype=t[n].dtype, pin_memory=True) for n in ins}
+    for n in ins:
+        h_in[n].copy_(t[n])
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items() if v is not None}
+    h_out["lse"] = torch.empty(lse_shape, dtype=torch.float32, pin_memory=True)
+    d_in = {n: torch.empty_like(t[n]) for n in ins}
+    ws = plan.workspace()
+
+    def e2e_step():
+        for n in ins:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        o, lse = plan.forward(d_in["q_b"], d_in["k_m"], d_in["v_m"], d_in["k_b"], d_in["v_b"], workspace=ws)
+        g = plan.backward(d_in["q_b"], d_in["k_m"], d_in["v_m"], d_in["k_b"], d_in["v_b"], o, lse, d_in["d_o"],
+                          workspace=ws)
+        h_out["o"].copy_(o, non_blocking=True)
+        h_out["lse"].copy_(lse, non_blocking=True)
+        for k in ("dq_b", "dk_m", "dv_m", "dk_b", "dv_b"):
+            h_out[k].copy_(g[k], non_blocking=True)
+        torch.cuda.synchronize()
+
+    e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    dt = (time.perf_counter() - t0) / args.e2e_steps
+    dt = max_over_ranks(dt, world)
+    flops = info["fwd_flops"] + info["bwd_flops"]
+    return {"value": world * flops / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": in_bytes,
+            "d2h_bytes_per_step": out_bytes, "ms_per_step": dt * 1e3, "steps": args.e2e_steps}
+
+
+# --------------------------------------------------------------------------- reference arm
+
+
+def run_reference(args, rank, world):
+    import torch
+    from branch_attention_speculative_gb300 import workloads as W
+    wl = W.config(args.config)
+    t = W.make_tensors(wl, device="cuda")
+    budget = args.ref_step_s
+    vals, units_total, secs_total = [], 0, 0.0
+    for i in range(args.warmup + args.steps):
+        tf, units, secs = oracle_sample(wl, t, budget, seed=100 + i, max_units=64)
+        if i >= args.warmup:
+            vals.append((tf, units, secs))
+            units_total += units
+            secs_total += secs
+    value = sum(v[0] * v[2] for v in vals) / max(secs_total, 1e-9)
+    ms = secs_total / max(args.steps, 1) * 1e3
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 inputs, upcast to fp64)",
+        "config": {"workload": wl.name, "family": wl.family, "tokens": wl.tokens, "ttt_depth": wl.depth,
+                   "heads_q": wl.heads_q, "heads_kv": wl.heads_kv, "head_dim": wl.head_dim, "cp_virtual": wl.cp},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": f"{units_total} seeded anchor units over {args.steps} steps "
+                                   f"(~{budget:.0f} s of fp64 numpy each), fwd+bwd rows"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=5, help="measured shape 1..5 (5 = 256K TTT, the headline)")
+    ap.add_argument("--e2e-steps", type=int, default=1)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-step-s", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    from branch_attention_speculative_gb300 import build as B
+    if rank == 0:
+        B.build()
+    barrier(world)
+    if world > 1 and rank != 0:
+        B.build()  # no-op once rank 0 has built; loads the same library
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,383 @@
+// C ABI of libba.so: argument checks, workspace carving, table upload and the
+// launch sequence of the forward and backward passes.  See include/ba.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "kernels.h"
+#include "plan.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e) {
+  std::strncpy(g_last_cuda_error, cudaGetErrorString(e), sizeof(g_last_cuda_error) - 1);
+  return BA_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool ok_tensor(const void* p) { return p != nullptr && aligned(p, 16); }
+
+unsigned char* ws_at(void* ws, size_t off) { return static_cast<unsigned char*>(ws) + off; }
+
+int check_ws(const ba_plan* p, void* ws, size_t bytes) {
+  if (!ws || !aligned(ws, 256) || bytes < p->ws.total) return BA_ERR_WORKSPACE;
+  return BA_OK;
+}
+
+BaTables device_tables(const ba_plan* p, void* ws) {
+  const BaWorkspaceLayout& w = p->ws;
+  unsigned char* t = ws_at(ws, w.tables);
+  BaTables tb{};
+  tb.row_lim = reinterpret_cast<const int32_t*>(t + w.t_row_lim);
+  tb.tok_perm = reinterpret_cast<const int32_t*>(t + w.t_tok_perm);
+  tb.anc_perm = reinterpret_cast<const int32_t*>(t + w.t_anc_perm);
+  tb.fq = reinterpret_cast<const BaQTile*>(t + w.t_fq);
+  tb.fseg = reinterpret_cast<const BaKvSeg*>(t + w.t_fseg);
+  tb.forder = reinterpret_cast<const int32_t*>(t + w.t_forder);
+  tb.bq = reinterpret_cast<const BaQTile*>(t + w.t_bq);
+  tb.bkv = reinterpret_cast<const BaKvTile*>(t + w.t_bkv);
+  tb.bqr = reinterpret_cast<const BaQRange*>(t + w.t_bqr);
+  tb.border = reinterpret_cast<const int32_t*>(t + w.t_border);
+  tb.n_fq = int32_t(p->fq.size());
+  tb.n_fseg = int32_t(p->fseg.size());
+  tb.n_bq = int32_t(p->bq.size());
+  tb.n_bkv = int32_t(p->bkv.size());
+  tb.n_bqr = int32_t(p->bqr.size());
+  tb.status = reinterpret_cast<unsigned int*>(ws_at(ws, w.status));
+  return tb;
+}
+
+// Resets the status word and uploads the plan's tables into the workspace.
+cudaError_t prepare(const ba_plan* p, void* ws, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(ws_at(ws, p->ws.status), 0, 256, st);
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyAsync(ws_at(ws, p->ws.tables), p->image.data(), p->ws.table_bytes, cudaMemcpyHostToDevice, st);
+}
+
+// Role geometry for the zigzag gather: outer count, units, unit bytes, permutation.
+struct Role {
+  int64_t outer, units, unit_bytes;
+  const int32_t* perm;
+};
+
+Role role_of(const ba_plan* p, const BaTables& tb, int role) {
+  const BaShape& sh = p->shape;
+  const bool block = sh.family == BA_FAMILY_BLOCK;
+  const int64_t d2 = int64_t(sh.d) * 2;
+  switch (role) {
+    case 0:
+      return block ? Role{1, p->NA, int64_t(sh.B) * sh.Hq * d2, tb.anc_perm}
+                   : Role{sh.steps, sh.T, int64_t(sh.Hq) * d2, tb.tok_perm};
+    case 1:
+      return Role{1, sh.T, int64_t(sh.Hkv) * d2, tb.tok_perm};
+    default:
+      if (sh.family == BA_FAMILY_CAUSAL) return Role{0, 0, 0, tb.tok_perm};
+      return block ? Role{1, p->NA, int64_t(sh.B) * sh.Hkv * d2, tb.anc_perm}
+                   : Role{sh.steps, sh.T, int64_t(sh.Hkv) * d2, tb.tok_perm};
+  }
+}
+
+cudaError_t pack(const ba_plan* p, const BaTables& tb, int role, const void* src, void* dst, int inverse,
+                 cudaStream_t st) {
+  const Role r = role_of(p, tb, role);
+  return ba_launch_zigzag_gather(src, dst, r.perm, r.outer, r.units, r.unit_bytes, inverse, st);
+}
+
+#define BA_TRY(x)                              \
+  do {                                         \
+    cudaError_t e_ = (x);                      \
+    if (e_ != cudaSuccess) return cuda_fail(e_); \
+  } while (0)
+
+enum KernelId { K_PACK = 0, K_MAIN_FWD, K_BRANCH_FWD, K_MERGE, K_BWD_PREP, K_MAIN_BWD, K_BRANCH_BWD, K_COUNT };
+const char* const kKernelNames[K_COUNT] = {"zigzag_pack", "main_fwd", "branch_fwd", "lse_merge",
+                                           "bwd_prep",    "main_bwd", "branch_bwd"};
+
+// Records an event pair around one launch when profiling is on.
+template <class F>
+cudaError_t timed(ba_plan* p, int kid, cudaStream_t st, F&& launch) {
+  if (!p->prof_on) return launch();
+  const size_t i = p->prof_used;
+  while (p->prof_events.size() < 2 * (i + 1)) {
+    cudaEvent_t e;
+    cudaError_t err = cudaEventCreate(&e);
+    if (err != cudaSuccess) return err;
+    p->prof_events.push_back(e);
+  }
+  auto* a = static_cast<cudaEvent_t>(p->prof_events[2 * i]);
+  auto* b = static_cast<cudaEvent_t>(p->prof_events[2 * i + 1]);
+  cudaError_t err = cudaEventRecord(a, st);
+  if (err != cudaSuccess) return err;
+  err = launch();
+  if (err != cudaSuccess) return err;
+  err = cudaEventRecord(b, st);
+  if (err != cudaSuccess) return err;
+  p->prof_kernel.push_back(kid);
+  p->prof_used = i + 1;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+ba_plan::~ba_plan() {
+  for (void* e : prof_events) cudaEventDestroy(static_cast<cudaEvent_t>(e));
+}
+
+extern "C" {
+
+int ba_plan_create(const ba_plan_desc* desc, ba_plan_t* out) {
+  if (!out) return BA_ERR_INVALID_ARG;
+  *out = nullptr;
+  ba_plan* p = new (std::nothrow) ba_plan();
+  if (!p) return BA_ERR_HOST_ALLOC;
+  int rc;
+  try {
+    rc = ba_build_plan(desc, p);
+  } catch (const std::bad_alloc&) {
+    rc = BA_ERR_HOST_ALLOC;
+  } catch (...) {
+    rc = BA_ERR_INVALID_ARG;
+  }
+  if (rc != BA_OK) {
+    delete p;
+    return rc;
+  }
+  *out = p;
+  return BA_OK;
+}
+
+void ba_plan_destroy(ba_plan_t plan) { delete plan; }
+
+int ba_plan_validate(ba_plan_t p) {
+  if (!p) return BA_ERR_INVALID_ARG;
+  try {
+    return ba_validate_plan(p);
+  } catch (...) {
+    return BA_ERR_HOST_ALLOC;
+  }
+}
+
+int ba_plan_get_info(ba_plan_t p, ba_plan_info* info) {
+  if (!p || !info) return BA_ERR_INVALID_ARG;
+  const BaShape& sh = p->shape;
+  info->main_tokens = sh.T;
+  info->branch_queries = int64_t(sh.steps) * sh.rows;
+  info->query_rows = info->branch_queries * sh.Hq;
+  info->main_pairs = p->main_pairs;
+  info->branch_pairs = p->branch_pairs;
+  info->fwd_flops = 4.0 * sh.d * double(p->main_pairs + p->branch_pairs);
+  info->bwd_flops = 2.5 * info->fwd_flops;
+  info->fwd_tiles = int64_t(p->fq.size());
+  info->fwd_tile_blocks = p->fwd_blocks;
+  info->bwd_kv_tiles = int64_t(p->bkv.size());
+  int64_t mx = 0;
+  for (int64_t v : p->comm) mx = v > mx ? v : mx;
+  info->comm_bytes_fwd_per_rank = mx;
+  info->workspace_bytes = int64_t(p->ws.total);
+  return BA_OK;
+}
+
+int ba_plan_get_table(ba_plan_t p, int32_t which, int32_t* out, int64_t capacity, int64_t* count) {
+  if (!p) return BA_ERR_INVALID_ARG;
+  const std::vector<int32_t>* v = nullptr;
+  switch (which) {
+    case BA_TABLE_TOKEN_PERM: v = &p->tok_perm; break;
+    case BA_TABLE_ANCHOR_PERM: v = &p->anc_perm; break;
+    case BA_TABLE_ROW_LIMIT: v = &p->row_lim; break;
+    case BA_TABLE_TOKEN_RANK: v = &p->tok_rank; break;
+    default: return BA_ERR_INVALID_ARG;
+  }
+  if (count) *count = int64_t(v->size());
+  if (!out) return BA_OK;
+  if (capacity < int64_t(v->size())) return BA_ERR_INVALID_ARG;
+  if (!v->empty()) std::memcpy(out, v->data(), v->size() * sizeof(int32_t));
+  return BA_OK;
+}
+
+int ba_plan_get_comm_volume(ba_plan_t p, int64_t* out, int32_t capacity) {
+  if (!p || !out || capacity < p->C) return BA_ERR_INVALID_ARG;
+  for (int r = 0; r < p->C; ++r) out[r] = p->comm[r];
+  return BA_OK;
+}
+
+size_t ba_workspace_bytes(ba_plan_t p) { return p ? p->ws.total : 0; }
+
+int ba_forward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, const void* k_b, const void* v_b,
+               void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!p) return BA_ERR_INVALID_ARG;
+  const bool has_b = p->shape.family != BA_FAMILY_CAUSAL;
+  if (!ok_tensor(q_b) || !ok_tensor(k_m) || !ok_tensor(v_m) || !ok_tensor(o) || !ok_tensor(lse))
+    return BA_ERR_INVALID_ARG;
+  if (has_b && (!ok_tensor(k_b) || !ok_tensor(v_b))) return BA_ERR_INVALID_ARG;
+  if (int rc = check_ws(p, workspace, workspace_bytes)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const BaWorkspaceLayout& w = p->ws;
+  BA_TRY(prepare(p, workspace, st));
+  BaFwdArgs a{};
+  a.sh = p->shape;
+  a.tb = device_tables(p, workspace);
+  a.qp = ws_at(workspace, w.qp);
+  a.kmp = ws_at(workspace, w.kmp);
+  a.vmp = ws_at(workspace, w.vmp);
+  a.kbp = ws_at(workspace, w.kbp);
+  a.vbp = ws_at(workspace, w.vbp);
+  a.om = reinterpret_cast<float*>(ws_at(workspace, w.om));
+  a.lm = reinterpret_cast<float*>(ws_at(workspace, w.lm));
+  a.ob = reinterpret_cast<float*>(ws_at(workspace, w.ob));
+  a.lb = reinterpret_cast<float*>(ws_at(workspace, w.lb));
+  a.o = o;
+  a.lse = lse;
+  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 0, q_b, const_cast<void*>(a.qp), 0, st); }));
+  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 1, k_m, const_cast<void*>(a.kmp), 0, st); }));
+  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 1, v_m, const_cast<void*>(a.vmp), 0, st); }));
+  if (has_b) {
+    BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, k_b, const_cast<void*>(a.kbp), 0, st); }));
+    BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, v_b, const_cast<void*>(a.vbp), 0, st); }));
+  }
+  BA_TRY(timed(p, K_MAIN_FWD, st, [&] { return ba_launch_main_fwd(a, st); }));
+  if (has_b) BA_TRY(timed(p, K_BRANCH_FWD, st, [&] { return ba_launch_branch_fwd(a, st); }));
+  BA_TRY(timed(p, K_MERGE, st, [&] { return ba_launch_merge_plan(a, st); }));
+  return BA_OK;
+}
+
+int ba_backward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, const void* k_b, const void* v_b,
+                const void* o, const float* lse, const void* d_o, void* dq_b, void* dk_m, void* dv_m, void* dk_b,
+                void* dv_b, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!p) return BA_ERR_INVALID_ARG;
+  const bool has_b = p->shape.family != BA_FAMILY_CAUSAL;
+  if (!ok_tensor(q_b) || !ok_tensor(k_m) || !ok_tensor(v_m) || !ok_tensor(o) || !ok_tensor(lse) ||
+      !ok_tensor(d_o) || !ok_tensor(dq_b) || !ok_tensor(dk_m) || !ok_tensor(dv_m))
+    return BA_ERR_INVALID_ARG;
+  if (has_b && (!ok_tensor(k_b) || !ok_tensor(v_b) || !ok_tensor(dk_b) || !ok_tensor(dv_b)))
+    return BA_ERR_INVALID_ARG;
+  if (int rc = check_ws(p, workspace, workspace_bytes)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const BaWorkspaceLayout& w = p->ws;
+  BA_TRY(prepare(p, workspace, st));
+  BaBwdArgs a{};
+  a.sh = p->shape;
+  a.tb = device_tables(p, workspace);
+  a.qp = ws_at(workspace, w.qp);
+  a.kmp = ws_at(workspace, w.kmp);
+  a.vmp = ws_at(workspace, w.vmp);
+  a.kbp = ws_at(workspace, w.kbp);
+  a.vbp = ws_at(workspace, w.vbp);
+  a.o = o;
+  a.d_o = d_o;
+  a.lse = lse;
+  a.dop = ws_at(workspace, w.dop);
+  a.dlt = reinterpret_cast<float*>(ws_at(workspace, w.dlt));
+  a.lsep = reinterpret_cast<float*>(ws_at(workspace, w.lsep));
+  a.dqacc = reinterpret_cast<float*>(ws_at(workspace, w.dqacc));
+  a.dq = dq_b;
+  a.dkm = dk_m;
+  a.dvm = dv_m;
+  a.dkb = dk_b;
+  a.dvb = dv_b;
+  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 0, q_b, const_cast<void*>(a.qp), 0, st); }));
+  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 1, k_m, const_cast<void*>(a.kmp), 0, st); }));
+  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 1, v_m, const_cast<void*>(a.vmp), 0, st); }));
+  if (has_b) {
+    BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, k_b, const_cast<void*>(a.kbp), 0, st); }));
+    BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, v_b, const_cast<void*>(a.vbp), 0, st); }));
+  }
+  BA_TRY(timed(p, K_BWD_PREP, st, [&] { return ba_launch_bwd_prep(a, st); }));
+  BA_TRY(timed(p, K_MAIN_BWD, st, [&] { return ba_launch_main_bwd(a, st); }));
+  BA_TRY(timed(p, K_BRANCH_BWD, st, [&] { return ba_launch_branch_bwd(a, st); }));
+  return BA_OK;
+}
+
+int ba_check_device_status(ba_plan_t p, void* workspace, void* stream) {
+  if (!p || !workspace) return BA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  BA_TRY(cudaStreamSynchronize(st));
+  unsigned int word = 0;
+  BA_TRY(cudaMemcpy(&word, ws_at(workspace, p->ws.status), sizeof(word), cudaMemcpyDeviceToHost));
+  if (word != 0) BA_TRY(cudaMemset(ws_at(workspace, p->ws.status), 0, sizeof(word)));
+  switch (word) {
+    case BA_DEV_OK: return BA_OK;
+    case BA_DEV_TIMEOUT: return BA_ERR_DEVICE_TIMEOUT;
+    default: return BA_ERR_DEVICE_BOUNDS;
+  }
+}
+
+int ba_zigzag_pack(ba_plan_t p, int32_t role, const void* src, void* dst, int32_t inverse, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (!p || role < 0 || role > 2 || !ok_tensor(src) || !ok_tensor(dst) || src == dst) return BA_ERR_INVALID_ARG;
+  if (role == 2 && p->shape.family == BA_FAMILY_CAUSAL) return BA_ERR_INVALID_ARG;
+  if (int rc = check_ws(p, workspace, workspace_bytes)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  BA_TRY(prepare(p, workspace, st));
+  BA_TRY(pack(p, device_tables(p, workspace), role, src, dst, inverse ? 1 : 0, st));
+  return BA_OK;
+}
+
+int ba_lse_merge(int64_t rows, int32_t head_dim, const float* o_m, const float* l_m, const float* o_b,
+                 const float* l_b, void* o, float* l, void* stream) {
+  if (rows < 0 || (head_dim != 64 && head_dim != 128)) return BA_ERR_INVALID_ARG;
+  if (rows == 0) return BA_OK;
+  if (!ok_tensor(o_m) || !ok_tensor(o_b) || !ok_tensor(o) || !l_m || !l_b || !l) return BA_ERR_INVALID_ARG;
+  BA_TRY(ba_launch_merge_rows(rows, head_dim, o_m, l_m, o_b, l_b, o, l, static_cast<cudaStream_t>(stream)));
+  return BA_OK;
+}
+
+const char* ba_status_string(int s) {
+  switch (s) {
+    case BA_OK: return "ok";
+    case BA_ERR_INVALID_ARG: return "invalid argument";
+    case BA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case BA_ERR_CUDA: return "CUDA error";
+    case BA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case BA_ERR_DEVICE_BOUNDS: return "device table index out of range";
+    case BA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case BA_ERR_HOST_ALLOC: return "host allocation failed";
+    default: return "unknown status";
+  }
+}
+
+int ba_profile_enable(ba_plan_t p, int32_t enable) {
+  if (!p) return BA_ERR_INVALID_ARG;
+  p->prof_on = enable != 0;
+  return BA_OK;
+}
+
+int ba_profile_read(ba_plan_t p, ba_kernel_time* out, int32_t capacity, int32_t* count) {
+  if (!p) return BA_ERR_INVALID_ARG;
+  for (size_t i = 0; i < p->prof_used; ++i) {
+    auto* a = static_cast<cudaEvent_t>(p->prof_events[2 * i]);
+    auto* b = static_cast<cudaEvent_t>(p->prof_events[2 * i + 1]);
+    BA_TRY(cudaEventSynchronize(b));
+    float ms = 0.f;
+    BA_TRY(cudaEventElapsedTime(&ms, a, b));
+    p->prof_ms[p->prof_kernel[i]] += ms;
+    p->prof_launches[p->prof_kernel[i]] += 1;
+  }
+  p->prof_used = 0;
+  p->prof_kernel.clear();
+  int n = 0;
+  for (int k = 0; k < K_COUNT; ++k) {
+    if (p->prof_launches[k] == 0) continue;
+    if (out && n < capacity) {
+      std::memset(out[n].name, 0, sizeof(out[n].name));
+      std::strncpy(out[n].name, kKernelNames[k], sizeof(out[n].name) - 1);
+      out[n].launches = p->prof_launches[k];
+      out[n].total_ms = p->prof_ms[k];
+    }
+    ++n;
+    p->prof_ms[k] = 0;
+    p->prof_launches[k] = 0;
+  }
+  if (count) *count = n;
+  return BA_OK;
+}
+
+const char* ba_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* ba_version(void) { return "0.1 sm_103a"; }
+
+}  // extern "C"

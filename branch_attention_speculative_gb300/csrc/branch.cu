@@ -1,0 +1,247 @@
+// K3 / K7 — rank-local branch attention, forward and backward.
+//
+// "Online Draft Co-Training ...", ai.info summary, Key Contributions 1 and
+// "Methodology in Plain English": the branch part is small and lives on the
+// rank that owns the anchor, so it needs no communication; rainbus page, core
+// method: the backward accumulates gradients locally with no
+// branch-dependent traffic.  Key sets (paperlens walkthrough, Wall 1):
+//   TTT   — step-j query at anchor p sees branch keys (p, i), i <= j;
+//   BLOCK — each of the B queries of an anchor sees all B keys of the block.
+//
+// One CTA handles one anchor unit (a packed position for TTT, a packed anchor
+// for BLOCK) and one kv head: the unit's few branch keys are staged in shared
+// memory as fp32, each warp takes query rows, a lane owns d/32 columns, dot
+// products are warp-shuffle reductions.  The work is tiny next to the main
+// part and bound by HBM traffic of q, dO and the outputs.
+//
+// The backward also finishes dQ: the main part arrives in the fp32
+// accumulator, the branch part is added here and the sum is written as bf16
+// in natural order (the finalize step, fused).
+#include <math.h>
+
+#include "device.cuh"
+#include "kernels.h"
+
+namespace {
+
+__device__ __forceinline__ int rows_per_unit(const BaShape& sh) {
+  return sh.family == BA_FAMILY_TTT ? sh.steps : (sh.family == BA_FAMILY_BLOCK ? sh.B : 1);
+}
+
+// packed branch-key slot of key i of unit u
+__device__ __forceinline__ int64_t branch_slot(const BaShape& sh, int64_t u, int i) {
+  return sh.family == BA_FAMILY_TTT ? int64_t(i) * sh.T + u : u * sh.B + i;
+}
+
+// natural branch-key slot of key i of packed unit u
+__device__ __forceinline__ int64_t branch_slot_nat(const BaShape& sh, const BaTables& tb, int64_t u, int i) {
+  return sh.family == BA_FAMILY_TTT ? int64_t(i) * sh.T + tb.tok_perm[u] : int64_t(tb.anc_perm[u]) * sh.B + i;
+}
+
+// (step j, packed row r) of query qi of unit u
+__device__ __forceinline__ void unit_query(const BaShape& sh, int64_t u, int qi, int64_t& j, int64_t& r) {
+  if (sh.family == BA_FAMILY_TTT) { j = qi; r = u; }
+  else if (sh.family == BA_FAMILY_BLOCK) { j = 0; r = u * sh.B + qi; }
+  else { j = 0; r = u; }
+}
+
+__device__ __forceinline__ int keys_of_query(const BaShape& sh, int qi) {
+  return sh.family == BA_FAMILY_TTT ? qi + 1 : (sh.family == BA_FAMILY_BLOCK ? sh.B : 0);
+}
+
+template <int D>
+__device__ __forceinline__ void load_row(const __nv_bfloat16* p, int lane, float* x) {
+  constexpr int E = D / 32;
+  if constexpr (E == 4) {
+    const uint2 v = reinterpret_cast<const uint2*>(p)[lane];
+    const float2 a = unpack_bf16(v.x), b = unpack_bf16(v.y);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  } else {
+    const float2 a = unpack_bf16(reinterpret_cast<const uint32_t*>(p)[lane]);
+    x[0] = a.x; x[1] = a.y;
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* p, int lane, const float* x) {
+  constexpr int E = D / 32;
+  if constexpr (E == 4) {
+    uint2 v;
+    v.x = pack_bf16(x[0], x[1]);
+    v.y = pack_bf16(x[2], x[3]);
+    reinterpret_cast<uint2*>(p)[lane] = v;
+  } else {
+    reinterpret_cast<uint32_t*>(p)[lane] = pack_bf16(x[0], x[1]);
+  }
+}
+
+template <int D>
+__device__ void stage_keys(const BaShape& sh, const __nv_bfloat16* kb, const __nv_bfloat16* vb, int64_t u, int kvh,
+                           float* ks, float* vs) {
+  const int n = sh.nbk * D;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int i = e / D, c = e % D;
+    const int64_t off = (branch_slot(sh, u, i) * sh.Hkv + kvh) * D + c;
+    ks[e] = __bfloat162float(kb[off]);
+    vs[e] = __bfloat162float(vb[off]);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) branch_fwd_kernel(BaFwdArgs a) {
+  extern __shared__ float smem[];
+  constexpr int E = D / 32;
+  const BaShape& sh = a.sh;
+  float* ks = smem;
+  float* vs = smem + sh.nbk * D;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const auto* qp = static_cast<const __nv_bfloat16*>(a.qp);
+  const auto* kb = static_cast<const __nv_bfloat16*>(a.kbp);
+  const auto* vb = static_cast<const __nv_bfloat16*>(a.vbp);
+  const int64_t total = sh.units * sh.Hkv;
+  const int nq = rows_per_unit(sh) * sh.G;
+  for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+    const int64_t u = w / sh.Hkv;
+    const int kvh = int(w % sh.Hkv);
+    __syncthreads();
+    stage_keys<D>(sh, kb, vb, u, kvh, ks, vs);
+    __syncthreads();
+    for (int idx = warp; idx < nq; idx += nwarps) {
+      const int qi = idx / sh.G, g = idx % sh.G;
+      int64_t j, r;
+      unit_query(sh, u, qi, j, r);
+      const int64_t qrow = (j * sh.rows + r) * sh.Hq + kvh * sh.G + g;
+      float q[E], acc[E];
+      load_row<D>(qp + qrow * D, lane, q);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = 0.f;
+      float m = -INFINITY, l = 0.f;
+      const int nk = keys_of_query(sh, qi);
+      for (int i = 0; i < nk; ++i) {
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dot += q[e] * ks[i * D + lane * E + e];
+        const float s2 = warp_sum(dot) * sh.scale_log2;
+        const float mn = fmaxf(m, s2);
+        const float c = exp2f(m - mn);
+        const float p = exp2f(s2 - mn);
+        l = l * c + p;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = acc[e] * c + p * vs[i * D + lane * E + e];
+        m = mn;
+      }
+      const float inv = 1.f / l;
+      float* orow = a.ob + qrow * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) orow[e] = acc[e] * inv;
+      if (lane == 0) a.lb[qrow] = (m + log2f(l)) * BA_LN2;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
+  extern __shared__ float smem[];
+  constexpr int E = D / 32;
+  const BaShape& sh = a.sh;
+  float* ks = smem;
+  float* vs = ks + sh.nbk * D;
+  float* dks = vs + sh.nbk * D;
+  float* dvs = dks + sh.nbk * D;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const auto* qp = static_cast<const __nv_bfloat16*>(a.qp);
+  const auto* dop = static_cast<const __nv_bfloat16*>(a.dop);
+  const auto* kb = static_cast<const __nv_bfloat16*>(a.kbp);
+  const auto* vb = static_cast<const __nv_bfloat16*>(a.vbp);
+  auto* dq = static_cast<__nv_bfloat16*>(a.dq);
+  auto* dkb = static_cast<__nv_bfloat16*>(a.dkb);
+  auto* dvb = static_cast<__nv_bfloat16*>(a.dvb);
+  const int64_t total = sh.units * sh.Hkv;
+  const int nq = rows_per_unit(sh) * sh.G;
+  for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+    const int64_t u = w / sh.Hkv;
+    const int kvh = int(w % sh.Hkv);
+    __syncthreads();
+    if (sh.nbk > 0) {
+      stage_keys<D>(sh, kb, vb, u, kvh, ks, vs);
+      for (int e = threadIdx.x; e < sh.nbk * D; e += blockDim.x) { dks[e] = 0.f; dvs[e] = 0.f; }
+    }
+    __syncthreads();
+    for (int idx = warp; idx < nq; idx += nwarps) {
+      const int qi = idx / sh.G, g = idx % sh.G;
+      int64_t j, r;
+      unit_query(sh, u, qi, j, r);
+      const int64_t qrow = (j * sh.rows + r) * sh.Hq + kvh * sh.G + g;
+      float q[E], go[E], gq[E];
+      load_row<D>(qp + qrow * D, lane, q);
+      load_row<D>(dop + qrow * D, lane, go);
+#pragma unroll
+      for (int e = 0; e < E; ++e) gq[e] = a.dqacc[qrow * D + lane * E + e];
+      const float l2 = a.lsep[qrow] * BA_LOG2E;
+      const float delta = a.dlt[qrow];
+      const int nk = keys_of_query(sh, qi);
+      for (int i = 0; i < nk; ++i) {
+        float dot = 0.f, dpv = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          dot += q[e] * ks[i * D + lane * E + e];
+          dpv += go[e] * vs[i * D + lane * E + e];
+        }
+        const float s2 = warp_sum(dot) * sh.scale_log2;
+        const float dp = warp_sum(dpv);
+        const float p = exp2f(s2 - l2);
+        const float ds = p * (dp - delta);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          gq[e] += sh.scale * ds * ks[i * D + lane * E + e];
+          atomicAdd(&dks[i * D + lane * E + e], sh.scale * ds * q[e]);
+          atomicAdd(&dvs[i * D + lane * E + e], p * go[e]);
+        }
+      }
+      const int64_t nrow = (j * sh.rows + natural_row(sh, a.tb, r)) * sh.Hq + kvh * sh.G + g;
+      store_row_bf16<D>(dq + nrow * D, lane, gq);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < sh.nbk * D; e += blockDim.x) {
+      const int i = e / D, c = e % D;
+      const int64_t off = (branch_slot_nat(sh, a.tb, u, i) * sh.Hkv + kvh) * D + c;
+      dkb[off] = __float2bfloat16_rn(dks[e]);
+      dvb[off] = __float2bfloat16_rn(dvs[e]);
+    }
+  }
+}
+
+int64_t grid_for(int64_t total) {
+  const int64_t cap = 152 * 16;
+  return total < cap ? total : cap;
+}
+
+}  // namespace
+
+cudaError_t ba_launch_branch_fwd(const BaFwdArgs& a, cudaStream_t st) {
+  const int64_t total = a.sh.units * a.sh.Hkv;
+  if (total == 0 || a.sh.nbk == 0) return cudaSuccess;
+  const size_t smem = size_t(2) * a.sh.nbk * a.sh.d * sizeof(float);
+  if (a.sh.d == 128) {
+    cudaFuncSetAttribute(branch_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    branch_fwd_kernel<128><<<unsigned(grid_for(total)), 128, smem, st>>>(a);
+  } else {
+    cudaFuncSetAttribute(branch_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    branch_fwd_kernel<64><<<unsigned(grid_for(total)), 128, smem, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t ba_launch_branch_bwd(const BaBwdArgs& a, cudaStream_t st) {
+  const int64_t total = a.sh.units * a.sh.Hkv;
+  if (total == 0) return cudaSuccess;
+  const size_t smem = size_t(4) * a.sh.nbk * a.sh.d * sizeof(float);
+  if (a.sh.d == 128) {
+    cudaFuncSetAttribute(branch_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    branch_bwd_kernel<128><<<unsigned(grid_for(total)), 128, smem, st>>>(a);
+  } else {
+    cudaFuncSetAttribute(branch_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    branch_bwd_kernel<64><<<unsigned(grid_for(total)), 128, smem, st>>>(a);
+  }
+  return cudaGetLastError();
+}

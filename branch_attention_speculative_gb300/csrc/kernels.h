@@ -1,0 +1,46 @@
+// Kernel launchers (host side).  Each returns the launch's cudaError_t.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ba_internal.h"
+
+struct BaFwdArgs {
+  BaShape sh;
+  BaTables tb;
+  const void *qp, *kmp, *vmp, *kbp, *vbp;  // packed inputs (bf16)
+  float *om, *lm, *ob, *lb;                // packed partials (fp32)
+  void* o;                                 // natural output (bf16)
+  float* lse;                              // natural lse (fp32)
+};
+
+struct BaBwdArgs {
+  BaShape sh;
+  BaTables tb;
+  const void *qp, *kmp, *vmp, *kbp, *vbp;  // packed inputs (bf16)
+  const void *o, *d_o;                     // natural (bf16)
+  const float* lse;                        // natural (fp32)
+  void* dop;                               // packed dO (bf16)
+  float *dlt, *lsep, *dqacc;               // packed Delta, lse, dQ accumulator (fp32)
+  void *dq, *dkm, *dvm, *dkb, *dvb;        // natural gradients (bf16)
+};
+
+// K1: dst[o][i] = src[o][perm[i]] (inverse = 0) or dst[o][perm[i]] = src[o][i].
+cudaError_t ba_launch_zigzag_gather(const void* src, void* dst, const int32_t* perm, int64_t outer,
+                                    int64_t units, int64_t unit_bytes, int inverse, cudaStream_t st);
+// K2: causal main attention over each query tile's key segments -> O_m, l_m.
+cudaError_t ba_launch_main_fwd(const BaFwdArgs& a, cudaStream_t st);
+// K3: rank-local branch attention -> O_b, l_b.
+cudaError_t ba_launch_branch_fwd(const BaFwdArgs& a, cudaStream_t st);
+// K4: Eq. 2 merge, packed partials -> natural o, lse.
+cudaError_t ba_launch_merge_plan(const BaFwdArgs& a, cudaStream_t st);
+// K4 on caller buffers with no permutation.
+cudaError_t ba_launch_merge_rows(int64_t rows, int d, const float* om, const float* lm, const float* ob,
+                                 const float* lb, void* o, float* l, cudaStream_t st);
+// K5: Delta = rowsum(dO * O), pack dO / lse, zero the dQ accumulator.
+cudaError_t ba_launch_bwd_prep(const BaBwdArgs& a, cudaStream_t st);
+// K6: main-attention backward (key-stationary): dK_m, dV_m (natural), dQ into the accumulator.
+cudaError_t ba_launch_main_bwd(const BaBwdArgs& a, cudaStream_t st);
+// K7 (+K8): branch backward: dK_b, dV_b (natural); dQ = accumulator + branch part -> natural bf16.
+cudaError_t ba_launch_branch_bwd(const BaBwdArgs& a, cudaStream_t st);

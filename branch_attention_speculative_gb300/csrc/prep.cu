@@ -1,0 +1,74 @@
+// K5 — backward preprocessing.
+//
+// For every query-head row: Delta = <dO, O> in fp32 (the row term of the
+// softmax backward, dS = P * (dP - Delta)); dO and lse are gathered into the
+// packed zigzag order the main backward reads; the row of the fp32 dQ
+// accumulator is zeroed.  The pages only say that the backward replays the
+// ring ("Online Draft Co-Training ...", rainbus page, method step 5); Delta is
+// what that replay needs per row when P is recomputed from the merged lse.
+// HBM-bound: d/8 threads per row, 16-byte loads.
+#include "device.cuh"
+#include "kernels.h"
+
+namespace {
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(BaBwdArgs a) {
+  constexpr int TPR = D / 8;  // threads per row, 8 bf16 each
+  constexpr int RPB = 256 / TPR;
+  const BaShape& sh = a.sh;
+  const int sub = threadIdx.x % TPR;
+  const int64_t rows = int64_t(sh.steps) * sh.rows * sh.Hq;
+  const auto* o = static_cast<const uint4*>(a.o);
+  const auto* go = static_cast<const uint4*>(a.d_o);
+  auto* dop = static_cast<uint4*>(a.dop);
+  // block-uniform trip count: the shuffles below need every lane of the warp
+  for (int64_t base = int64_t(blockIdx.x) * RPB; base < rows; base += int64_t(gridDim.x) * RPB) {
+    const int64_t row = base + threadIdx.x / TPR;
+    const bool valid = row < rows;
+    const int64_t h = row % sh.Hq;
+    const int64_t jr = row / sh.Hq;
+    const int64_t j = jr / sh.rows;
+    const int64_t r = jr - j * sh.rows;
+    const int64_t nrow = valid ? (j * sh.rows + natural_row(sh, a.tb, r)) * sh.Hq + h : 0;
+    uint4 ov = make_uint4(0, 0, 0, 0), gv = make_uint4(0, 0, 0, 0);
+    if (valid) {
+      ov = o[nrow * TPR + sub];
+      gv = go[nrow * TPR + sub];
+    }
+    float acc = 0.f;
+    const uint32_t* ow = reinterpret_cast<const uint32_t*>(&ov);
+    const uint32_t* gw = reinterpret_cast<const uint32_t*>(&gv);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = unpack_bf16(ow[k]), y = unpack_bf16(gw[k]);
+      acc += x.x * y.x + x.y * y.y;
+    }
+#pragma unroll
+    for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (!valid) continue;
+    dop[row * TPR + sub] = gv;
+    float4* dq = reinterpret_cast<float4*>(a.dqacc + row * D);
+    dq[2 * sub] = make_float4(0.f, 0.f, 0.f, 0.f);
+    dq[2 * sub + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (sub == 0) {
+      a.dlt[row] = acc;
+      a.lsep[row] = a.lse[nrow];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t ba_launch_bwd_prep(const BaBwdArgs& a, cudaStream_t st) {
+  const int64_t rows = int64_t(a.sh.steps) * a.sh.rows * a.sh.Hq;
+  if (rows == 0) return cudaSuccess;
+  const int rpb = 256 / (a.sh.d / 8);
+  int64_t blocks = (rows + rpb - 1) / rpb;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  if (a.sh.d == 128)
+    bwd_prep_kernel<128><<<unsigned(blocks), 256, 0, st>>>(a);
+  else
+    bwd_prep_kernel<64><<<unsigned(blocks), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}

@@ -1,0 +1,223 @@
+/*
+ * ba.h — C ABI of the branch-attention library (libba.so), GB300 / sm_103a.
+ *
+ * Draft branch attention as decomposed in "Online Draft Co-Training for
+ * Speculative Decoding in Large-Scale, Long-Context RL Post-Training"
+ * (arXiv 2609.07108): every branch query attends (a) the causal prefix of its
+ * main sequence and (b) the keys of its own branch.  Part (a) is computed as
+ * causal attention over packed, load-balanced zigzag chunks (virtual
+ * context-parallel ranks visited in ring order), part (b) as rank-local
+ * attention over the branch keys, and the two are merged exactly by the
+ * online-softmax log-sum-exp reduction (Eq. 2).  Sources: ai.info summary,
+ * Key Contributions 1 and "Methodology in Plain English"; rainbus page, core
+ * method (Eq. 2, Eq. 3), method step 2 and step 5, Figure 1.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Plain C types only.  `stream` is a cudaStream_t passed as void* (NULL is
+ *   the legacy default stream).  Device pointers point into memory of the
+ *   current CUDA device; the library allocates no device memory and no
+ *   pinned memory on the compute calls: the caller owns every device buffer,
+ *   including the workspace.
+ * - Tensors are dense, contiguous, row-major, bf16 (2 bytes per element)
+ *   unless stated otherwise, 16-byte aligned.  "Natural" layouts:
+ *     TTT (EAGLE-3 Training-Time Test, depth D):
+ *         q_b, o, d_o, dq_b  [D][T][Hq][d]       lse  [D][T][Hq] fp32
+ *         k_b, v_b, dk_b, dv_b [D][T][Hkv][d]
+ *     BLOCK (DFlash / DSpark, block size B, NA = num_seqs * A anchors, in the
+ *            order of the `anchors` array):
+ *         q_b, o, d_o, dq_b  [NA][B][Hq][d]      lse  [NA][B][Hq] fp32
+ *         k_b, v_b, dk_b, dv_b [NA][B][Hkv][d]
+ *     CAUSAL (main queries, no branch keys):
+ *         q_b, o, d_o, dq_b  [1][T][Hq][d]       lse  [1][T][Hq] fp32
+ *         k_b, v_b, dk_b, dv_b unused (may be NULL)
+ *     main keys/values and their gradients k_m, v_m, dk_m, dv_m [T][Hkv][d].
+ *   lse is the natural-log log-sum-exp of scale * <q, k> over the query's
+ *   whole key set (main prefix and branch keys).
+ * - Query head h reads kv head h / (Hq / Hkv).
+ * - Calls are asynchronous on `stream`.  Argument errors are returned before
+ *   anything is enqueued.  Launch failures return BA_ERR_CUDA.  Device-side
+ *   faults that the kernels detect themselves (bounded waits that expire,
+ *   table indexes out of range) are recorded in a status word inside the
+ *   workspace and reported by ba_check_device_status.
+ * - No C++ exception crosses this boundary.
+ */
+#ifndef BA_H_
+#define BA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ba_plan* ba_plan_t;
+
+typedef enum {
+  BA_OK = 0,
+  BA_ERR_INVALID_ARG = -1,    /* bad descriptor, pointer, size or alignment  */
+  BA_ERR_UNSUPPORTED = -2,    /* valid but not built (e.g. head_dim 96)      */
+  BA_ERR_CUDA = -3,           /* a CUDA runtime call or launch failed         */
+  BA_ERR_DEVICE_TIMEOUT = -4, /* a bounded device wait expired                */
+  BA_ERR_DEVICE_BOUNDS = -5,  /* a kernel found a table index out of range    */
+  BA_ERR_WORKSPACE = -6,      /* workspace missing, too small or misaligned   */
+  BA_ERR_HOST_ALLOC = -7      /* host memory for the plan could not be had    */
+} ba_status;
+
+typedef enum {
+  BA_FAMILY_TTT = 0,    /* EAGLE-3 TTT: depth-D branch at every position       */
+  BA_FAMILY_BLOCK = 1,  /* DFlash / DSpark: B-token bidirectional block/anchor */
+  BA_FAMILY_CAUSAL = 2  /* main queries only: plain causal varlen attention    */
+} ba_family;
+
+/* Plan descriptor.  Host memory; copied by ba_plan_create. */
+typedef struct {
+  int32_t family;              /* ba_family                                      */
+  int32_t num_seqs;            /* S >= 1                                         */
+  const int32_t* cu_seqlens;   /* host [S+1]: 0 = cu[0] < cu[1] < ... = T        */
+  int32_t heads_q, heads_kv;   /* heads_q % heads_kv == 0                        */
+  int32_t head_dim;            /* 64 or 128                                      */
+  float softmax_scale;         /* usually 1/sqrt(head_dim)                       */
+  int32_t cp_degree;           /* virtual C >= 1; every length % (2C) == 0       */
+  int32_t ttt_depth;           /* TTT: D in [1, 16]                              */
+  int32_t block_size;          /* BLOCK: B in [1, 64]                            */
+  int32_t anchors_per_seq;     /* BLOCK: A >= 1                                  */
+  const int32_t* anchors;      /* BLOCK: host [S*A] absolute packed positions,
+                                  strictly ascending within each sequence and
+                                  inside it                                     */
+} ba_plan_desc;
+
+/* Figures a plan knows without running anything. */
+typedef struct {
+  int64_t main_tokens;          /* T                                            */
+  int64_t branch_queries;       /* D*T (TTT), NA*B (BLOCK), T (CAUSAL)           */
+  int64_t query_rows;           /* branch_queries * Hq                          */
+  int64_t main_pairs;           /* unmasked (query-head row, main key) pairs     */
+  int64_t branch_pairs;         /* unmasked (query-head row, branch key) pairs   */
+  double fwd_flops;             /* 4 * d * (main_pairs + branch_pairs)           */
+  double bwd_flops;             /* 2.5 * fwd_flops (recompute of S included)     */
+  int64_t fwd_tiles;            /* main-attention query tiles (per stream)       */
+  int64_t fwd_tile_blocks;      /* key blocks those tiles visit (per stream)     */
+  int64_t bwd_kv_tiles;         /* main-attention key tiles (per kv head)        */
+  int64_t comm_bytes_fwd_per_rank; /* Eq. 3 volume the ring would move (max rank) */
+  int64_t workspace_bytes;      /* = ba_workspace_bytes(plan)                    */
+} ba_plan_info;
+
+/* Tables a plan can copy out (host) for inspection and tests. */
+typedef enum {
+  BA_TABLE_TOKEN_PERM = 0,   /* int32 [T]: packed token -> natural token         */
+  BA_TABLE_ANCHOR_PERM = 1,  /* int32 [NA]: packed anchor -> natural anchor index */
+  BA_TABLE_ROW_LIMIT = 2,    /* int32 [rows]: packed row -> last visible main pos */
+  BA_TABLE_TOKEN_RANK = 3    /* int32 [T]: natural token -> owning virtual rank   */
+} ba_table;
+
+/* Build a plan: zigzag chunk map (2C chunks per sequence, rank r holding
+ * chunks r and 2C-1-r; rainbus page, CP prerequisites, Figure 1(a)), anchor
+ * ownership (a branch lives on its anchor's rank), per-row key limits, the
+ * main-attention tile lists in ring order with fully masked tiles dropped,
+ * longest-first, and the Eq. 3 volume.  Host only: launches nothing and needs
+ * no GPU.  On success *out owns host memory freed by ba_plan_destroy.
+ * Errors: BA_ERR_INVALID_ARG (descriptor), BA_ERR_UNSUPPORTED (head_dim),
+ * BA_ERR_HOST_ALLOC. */
+int ba_plan_create(const ba_plan_desc* desc, ba_plan_t* out);
+void ba_plan_destroy(ba_plan_t plan);
+/* Host self-check of a plan: every table index the kernels follow lies
+ * inside the buffer it addresses, permutations are permutations, unmasked
+ * key segments really are below every row limit of their tile.  BA_OK or
+ * BA_ERR_INVALID_ARG. */
+int ba_plan_validate(ba_plan_t plan);
+int ba_plan_get_info(ba_plan_t plan, ba_plan_info* info);
+/* Copies table `which` into host `out` (capacity in elements); *count gets the
+ * table length.  BA_ERR_INVALID_ARG if out is too small. */
+int ba_plan_get_table(ba_plan_t plan, int32_t which, int32_t* out, int64_t capacity,
+                      int64_t* count);
+
+/* Eq. 3 forward volume per virtual rank (rainbus page, core method):
+ * the bytes of main K and V that rank r would receive over the C-1 ring steps,
+ * counted from the plan's schedule; branch keys never move.  out: host
+ * int64 [capacity >= C]. */
+int ba_plan_get_comm_volume(ba_plan_t plan, int64_t* out, int32_t capacity);
+
+/* Bytes of device workspace that ba_forward / ba_backward need (one size
+ * serves both).  The workspace must be 256-byte aligned and must not be used
+ * by two calls at once; consecutive calls may share it. */
+size_t ba_workspace_bytes(ba_plan_t plan);
+
+/* Forward (rainbus page, method step 2; Figure 1(b)).  Packs the inputs into
+ * zigzag order, runs causal main attention over each query tile's key chunks
+ * in ring order (online softmax merge between steps), rank-local branch
+ * attention, and the Eq. 2 merge, which writes o and lse in natural order.
+ * Inputs q_b, k_m, v_m, k_b, v_b; outputs o (bf16) and lse (fp32). */
+int ba_forward(ba_plan_t plan, const void* q_b, const void* k_m, const void* v_m,
+               const void* k_b, const void* v_b, void* o, float* lse,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward (rainbus page, method step 5: the ring is replayed and gradients
+ * accumulate locally; core method: no branch-dependent traffic).  Given the
+ * forward's o and lse and the output gradient d_o, writes dq_b, dk_m, dv_m,
+ * dk_b, dv_b (bf16, natural layouts).  P is recomputed from the merged lse,
+ * which is exact for both key sets because Eq. 2's merged result is the
+ * single softmax over their union. */
+int ba_backward(ba_plan_t plan, const void* q_b, const void* k_m, const void* v_m,
+                const void* k_b, const void* v_b, const void* o, const float* lse,
+                const void* d_o, void* dq_b, void* dk_m, void* dv_m, void* dk_b, void* dv_b,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, reads and clears the status word in `workspace`,
+ * and returns the first device-side error recorded since the word was last
+ * reset (BA_OK if none).  ba_forward, ba_backward and ba_zigzag_pack reset the
+ * word when they start, so check after the call whose faults you want. */
+int ba_check_device_status(ba_plan_t plan, void* workspace, void* stream);
+
+/* Zigzag pack (inverse = 0) or unpack (inverse = 1) of one tensor through the
+ * plan's permutation (rainbus page, CP prerequisites and method step 2: each
+ * rank's shard holds, sequence by sequence, chunk r then chunk 2C-1-r; the
+ * shards of ranks 0..C-1 are concatenated).  role 0: query-shaped (q_b, o,
+ * d_o); role 1: main K/V shaped; role 2: branch K/V shaped.  src and dst are
+ * distinct device buffers of that role's natural size.  The permutation is
+ * uploaded into `workspace` (ba_workspace_bytes bytes). */
+int ba_zigzag_pack(ba_plan_t plan, int32_t role, const void* src, void* dst, int32_t inverse,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Eq. 2 on caller buffers, row by row, no permutation (rainbus page, core
+ * method, Eq. 2):  l = log(e^l_m + e^l_b),
+ *   o = (e^(l_m-l) o_m + e^(l_b-l) o_b) / (e^(l_m-l) + e^(l_b-l)).
+ * o_m, o_b fp32 [rows][head_dim]; l_m, l_b fp32 [rows] (natural log; -inf
+ * marks an empty part, which merges as the identity; two empty parts give
+ * o = 0, l = -inf).  Outputs o bf16 [rows][head_dim], l fp32 [rows].
+ * head_dim in {64, 128}. */
+int ba_lse_merge(int64_t rows, int32_t head_dim, const float* o_m, const float* l_m,
+                 const float* o_b, const float* l_b, void* o, float* l, void* stream);
+
+/* Optional per-kernel timing.  While enabled, the library brackets each of
+ * its kernel launches inside ba_forward / ba_backward with a pair of CUDA
+ * events recorded on the launching stream (events are created by the library
+ * and reused; no device memory is allocated).  ba_profile_read waits for the
+ * recorded events, adds their elapsed times per kernel name since the last
+ * read, writes up to `capacity` entries and returns the entry count in
+ * *count.  Names: zigzag_pack, main_fwd, branch_fwd, lse_merge, bwd_prep,
+ * main_bwd, branch_bwd. */
+typedef struct {
+  char name[24];
+  int64_t launches;
+  double total_ms;
+} ba_kernel_time;
+int ba_profile_enable(ba_plan_t plan, int32_t enable);
+int ba_profile_read(ba_plan_t plan, ba_kernel_time* out, int32_t capacity, int32_t* count);
+
+/* Text of the last CUDA error this thread saw inside the library ("" if
+ * none); valid until the thread's next failing call. */
+const char* ba_last_cuda_error(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* ba_status_string(int status);
+
+/* Library version and the architecture it was built for, e.g. "0.1 sm_103a". */
+const char* ba_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BA_H_ */

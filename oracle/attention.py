@@ -175,89 +175,117 @@ def backward(wl, t, o=None, lse=None):
 # sampled evaluation (large workloads)
 
 
-def _unit_keys(wl, unit, km, vm, kb, vb, kh):
+class ArraySource:
+    """Input access for the sampled evaluators.  ``rows(name, ids)`` returns
+    flat rows of q_b / d_o (over Hq) or k_b / v_b (over Hkv) as fp64
+    [len(ids), H, d]; ``main(name, kh)`` returns the whole main k_m / v_m
+    column of kv head kh as fp64 [T, d].  This one reads in-memory arrays;
+    callers with inputs elsewhere supply an object with the same two methods."""
+
+    def __init__(self, wl, t):
+        self.wl = wl
+        self.t = t
+        self._main = {}
+
+    def rows(self, name, ids):
+        heads = self.wl.heads_q if name in ("q_b", "d_o") else self.wl.heads_kv
+        x = np.asarray(self.t[name])
+        return np.asarray(x.reshape(-1, heads, x.shape[-1])[np.asarray(ids)], dtype=np.float64)
+
+    def main(self, name, kh):
+        key = (name, kh)
+        if key not in self._main:
+            self._main[key] = np.asarray(np.asarray(self.t[name])[:, kh], dtype=np.float64)
+        return self._main[key]
+
+
+def _as_source(wl, src):
+    return src if hasattr(src, "rows") and hasattr(src, "main") else ArraySource(wl, src)
+
+
+def _unit_span(wl, unit):
     p = keysets.unit_position(wl, unit)
     s = int(keysets.seq_of_position(wl.cu_seqlens, np.array([p]))[0])
-    a = int(wl.cu_seqlens[s])
-    kpos = np.arange(a, p + 1)
+    return int(wl.cu_seqlens[s]), p
+
+
+def _unit_problem(wl, src, unit, grads):
+    """Queries, key mask and inputs of one anchor unit."""
+    qids = keysets.queries_of_unit(wl, unit)
     bids = keysets.branch_keys_of_unit(wl, unit)
-    K = np.asarray(km[a:p + 1, kh], dtype=np.float64)
-    V = np.asarray(vm[a:p + 1, kh], dtype=np.float64)
-    if len(bids):
-        K = np.concatenate([K, np.asarray(kb[bids, kh], dtype=np.float64)], axis=0)
-        V = np.concatenate([V, np.asarray(vb[bids, kh], dtype=np.float64)], axis=0)
-    return kpos, bids, K, V
+    a, p = _unit_span(wl, unit)
+    kpos = np.arange(a, p + 1)
+    mask = np.concatenate([keysets.main_mask(wl, qids, kpos),
+                           keysets.branch_mask(wl, qids, bids)], axis=1)
+    causal = wl.family == "causal"
+    return dict(qids=qids, bids=bids, a=a, p=p, kpos=kpos, mask=mask, Q=src.rows("q_b", qids),
+                dO=src.rows("d_o", qids) if grads else None,
+                Kb=None if causal else src.rows("k_b", bids), Vb=None if causal else src.rows("v_b", bids))
 
 
-def unit_eval(wl, t, units, heads=None, grads=True):
+def _unit_kv(wl, src, u, kh):
+    K = src.main("k_m", kh)[u["a"]:u["p"] + 1]
+    V = src.main("v_m", kh)[u["a"]:u["p"] + 1]
+    if u["Kb"] is not None:
+        K = np.concatenate([K, u["Kb"][:, kh]], axis=0)
+        V = np.concatenate([V, u["Vb"][:, kh]], axis=0)
+    return K, V
+
+
+def unit_eval(wl, src, units, heads=None, grads=True):
     """Row-local evaluation of every query hanging from the given anchor
     units (positions for TTT/causal, anchor indices for block), restricted to
-    the listed q heads.  Each query's key set is built from its own unit, so
-    the cost is one row block per (unit, head).
+    the listed q heads.  Each query's key set is built from its own unit:
+    main keys [seq_start, p] and the unit's branch keys, with the mask of
+    ``keysets`` applied over them.
 
-    Returns dict with, per unit, arrays indexed [query-in-unit, head-in-list]:
-    o, lse and (if grads) dq, plus the unit's branch-key gradients dk_b,
-    dv_b [branch-key-in-unit, kv head] accumulated over the listed heads."""
+    ``src`` is an ``ArraySource`` (or a dict of natural-layout arrays).
+    Returns one dict per unit with arrays indexed [query-in-unit,
+    head-in-list]: o, lse and (if grads) dq, plus the unit's branch-key
+    gradients dk_b, dv_b [branch-key-in-unit, kv head] summed over the listed
+    heads."""
+    src = _as_source(wl, src)
     heads = list(range(wl.heads_q)) if heads is None else list(heads)
-    q = _flat(t["q_b"], wl.heads_q)
-    do = _flat(t["d_o"], wl.heads_q) if grads else None
-    km, vm = t["k_m"], t["v_m"]
-    causal = wl.family == "causal"
-    kb = None if causal else _flat(t["k_b"], wl.heads_kv)
-    vb = None if causal else _flat(t["v_b"], wl.heads_kv)
     G = _group(wl)
     res = []
     for unit in units:
-        qids = keysets.queries_of_unit(wl, int(unit))
-        nq = len(qids)
-        entry = {
-            "unit": int(unit),
-            "qids": qids,
-            "o": np.zeros((nq, len(heads), wl.head_dim)),
-            "lse": np.zeros((nq, len(heads))),
-        }
-        nb = len(keysets.branch_keys_of_unit(wl, int(unit)))
+        u = _unit_problem(wl, src, int(unit), grads)
+        nq, nb = len(u["qids"]), len(u["bids"])
+        entry = {"unit": int(unit), "qids": u["qids"],
+                 "o": np.zeros((nq, len(heads), wl.head_dim)), "lse": np.zeros((nq, len(heads)))}
         if grads:
             entry["dq"] = np.zeros((nq, len(heads), wl.head_dim))
             entry["dk_b"] = np.zeros((nb, wl.heads_kv, wl.head_dim))
             entry["dv_b"] = np.zeros((nb, wl.heads_kv, wl.head_dim))
         for hi, h in enumerate(heads):
             kh = h // G
-            kpos, bids, K, V = _unit_keys(wl, int(unit), km, vm, kb, vb, kh)
-            mask = np.concatenate([keysets.main_mask(wl, qids, kpos),
-                                   keysets.branch_mask(wl, qids, bids)], axis=1)
-            Q = q[qids, h]
-            oo, ll = masked_attention_fwd(Q, K, V, mask, wl.scale)
+            K, V = _unit_kv(wl, src, u, kh)
+            oo, ll = masked_attention_fwd(u["Q"][:, h], K, V, u["mask"], wl.scale)
             entry["o"][:, hi] = oo
             entry["lse"][:, hi] = ll
             if grads:
-                gq, gk, gv = masked_attention_bwd(Q, K, V, mask, wl.scale, oo, ll, do[qids, h])
+                gq, gk, gv = masked_attention_bwd(u["Q"][:, h], K, V, u["mask"], wl.scale, oo, ll, u["dO"][:, h])
                 entry["dq"][:, hi] = gq
-                n_main = len(kpos)
+                n_main = len(u["kpos"])
                 entry["dk_b"][:, kh] += gk[n_main:]
                 entry["dv_b"][:, kh] += gv[n_main:]
         res.append(entry)
     return res
 
 
-def main_key_grads(wl, t, key_lo: int, key_hi: int, kv_heads=None):
+def main_key_grads(wl, src, key_lo: int, key_hi: int, kv_heads=None):
     """dK_m, dV_m for the main keys [key_lo, key_hi) (one sequence), summed
     over every query that attends them.  Each attending query's lse and O come
     from its own full key set (row-local forward), so the cost is bounded by
     the number of queries anchored at or after key_lo.
 
     Returns (dk [key_hi-key_lo, len(kv_heads), d], dv likewise)."""
+    src = _as_source(wl, src)
     kv_heads = list(range(wl.heads_kv)) if kv_heads is None else list(kv_heads)
     cu = np.asarray(wl.cu_seqlens, dtype=np.int64)
     s = int(keysets.seq_of_position(cu, np.array([key_lo]))[0])
     if key_hi > cu[s + 1]:
         raise ValueError("window crosses a sequence end")
-    q = _flat(t["q_b"], wl.heads_q)
-    do = _flat(t["d_o"], wl.heads_q)
-    km, vm = t["k_m"], t["v_m"]
-    causal = wl.family == "causal"
-    kb = None if causal else _flat(t["k_b"], wl.heads_kv)
-    vb = None if causal else _flat(t["v_b"], wl.heads_kv)
     G = _group(wl)
     n = key_hi - key_lo
     dk = np.zeros((n, len(kv_heads), wl.head_dim))
@@ -269,20 +297,16 @@ def main_key_grads(wl, t, key_lo: int, key_hi: int, kv_heads=None):
     else:
         units = np.arange(key_lo, cu[s + 1])
     for unit in units:
-        qids = keysets.queries_of_unit(wl, int(unit))
+        u = _unit_problem(wl, src, int(unit), True)
+        a, p = u["a"], u["p"]
+        m = min(p + 1, key_hi) - key_lo  # window keys this unit sees
         for ki, kh in enumerate(kv_heads):
-            kpos, bids, K, V = _unit_keys(wl, int(unit), km, vm, kb, vb, kh)
-            mask = np.concatenate([keysets.main_mask(wl, qids, kpos),
-                                   keysets.branch_mask(wl, qids, bids)], axis=1)
-            sel = slice(key_lo - int(kpos[0]), key_hi - int(kpos[0]))
+            K, V = _unit_kv(wl, src, u, kh)
             for h in range(kh * G, (kh + 1) * G):
-                Q = q[qids, h]
-                oo, ll = masked_attention_fwd(Q, K, V, mask, wl.scale)
-                _, gk, gv = masked_attention_bwd(Q, K, V, mask, wl.scale, oo, ll, do[qids, h])
-                m = min(len(kpos), key_hi - int(kpos[0])) - (key_lo - int(kpos[0]))
-                if m > 0:
-                    dk[:m, ki] += gk[sel][:m]
-                    dv[:m, ki] += gv[sel][:m]
+                oo, ll = masked_attention_fwd(u["Q"][:, h], K, V, u["mask"], wl.scale)
+                _, gk, gv = masked_attention_bwd(u["Q"][:, h], K, V, u["mask"], wl.scale, oo, ll, u["dO"][:, h])
+                dk[:m, ki] += gk[key_lo - a:key_lo - a + m]
+                dv[:m, ki] += gv[key_lo - a:key_lo - a + m]
     return dk, dv
 
 

@@ -1,0 +1,144 @@
+"""Host-side checks of libba.so (no GPU launch): the exported C ABI, the
+planner's zigzag tables against the oracle's, useful-pair counts, Eq. 3, and
+descriptor validation."""
+
+import ctypes
+import re
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from branch_attention_speculative_gb300 import build as B
+from branch_attention_speculative_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def api():
+    B.build()
+    from branch_attention_speculative_gb300 import api as A
+    return A
+
+
+def header_symbols():
+    txt = open(os.path.join(ROOT, "include", "ba.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(ba_[a-z_]+)\s*\(", txt)))
+
+
+def test_library_exports_every_header_symbol(api):
+    lib = ctypes.CDLL(api.LIB_PATH)
+    syms = header_symbols()
+    assert len(syms) >= 12
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert sorted(api.exported_symbols()) == syms
+    assert api.version().endswith("sm_103a")
+
+
+def _cases():
+    return [W.config(1), W.config(2), W.config(3),
+            W.small("ttt", [16, 32, 48], cp=4, depth=2),
+            W.small("block", [64, 32], cp=2, block=4, anchors_per_seq=9, seed=3),
+            W.small("causal", [24, 8], cp=2)]
+
+
+@pytest.mark.parametrize("wl", _cases(), ids=lambda w: w.name)
+def test_zigzag_tables_match_oracle(api, wl):
+    p = api.Plan.from_workload(wl)
+    perm = oracle.zigzag.packed_token_order(wl.cu_seqlens, wl.cp)
+    assert np.array_equal(p.table("token_perm"), perm)
+    _, owner = oracle.zigzag.token_chunk(wl.cu_seqlens, wl.cp)
+    assert np.array_equal(p.table("token_rank"), owner)
+    if wl.family == "block":
+        ap = oracle.zigzag.packed_anchor_order(wl.cu_seqlens, wl.cp, wl.anchors)
+        assert np.array_equal(p.table("anchor_perm"), ap)
+        lim = np.repeat(np.asarray(wl.anchors)[ap], wl.block)
+    else:
+        lim = perm
+    assert np.array_equal(p.table("row_limit"), lim)
+
+
+@pytest.mark.parametrize("wl", _cases(), ids=lambda w: w.name)
+def test_useful_pairs_and_eq3_match_oracle(api, wl):
+    p = api.Plan.from_workload(wl)
+    inf = p.info()
+    if wl.tokens <= 4096:
+        assert inf["main_pairs"] + inf["branch_pairs"] == oracle.attention.useful_pairs(wl)
+    vol = oracle.zigzag.comm_volume_fwd(wl.cu_seqlens, wl.cp, wl.heads_kv, wl.head_dim, 2)
+    assert np.array_equal(p.comm_volume(), vol)
+    assert inf["fwd_flops"] == 4 * wl.head_dim * (inf["main_pairs"] + inf["branch_pairs"])
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 5])
+def test_measured_shape_plans_validate(api, k):
+    api.Plan.from_workload(W.config(k)).validate()
+
+
+@pytest.mark.parametrize("wl", _cases(), ids=lambda w: w.name)
+def test_small_plans_validate(api, wl):
+    api.Plan.from_workload(wl).validate()
+
+
+def test_comm_volume_does_not_depend_on_branches(api):
+    # Eq. 3: the same main sequence with and without branches moves the same bytes
+    lens = [64, 128]
+    vols = []
+    for fam, kw in (("causal", {}), ("ttt", {"depth": 5}), ("block", {"block": 8, "anchors_per_seq": 7})):
+        wl = W.small(fam, lens, cp=4, **kw)
+        vols.append(api.Plan.from_workload(wl).comm_volume())
+    assert all(np.array_equal(v, vols[0]) for v in vols)
+
+
+def test_config5_pairs_closed_form(api):
+    wl = W.config(5)
+    inf = api.Plan.from_workload(wl).info()
+    T = wl.tokens
+    assert inf["main_pairs"] == 32 * 7 * (T * (T + 1) // 2)
+    assert inf["branch_pairs"] == 32 * (7 * 8 // 2) * T
+
+
+@pytest.mark.parametrize("bad", [
+    dict(cp=3),                       # 256 not a multiple of 6
+    dict(heads_q=3, heads_kv=2),      # not a GQA group
+    dict(head_dim=0),
+    dict(depth=0),
+    dict(depth=17),
+])
+def test_bad_descriptors_rejected(api, bad):
+    kw = dict(family="ttt", cu_seqlens=[0, 256], heads_q=2, heads_kv=1, head_dim=64, cp=2, ttt_depth=3)
+    if "depth" in bad:
+        kw["ttt_depth"] = bad.pop("depth")
+    kw.update(bad)
+    with pytest.raises(api.BaError) as e:
+        api.Plan(**kw)
+    assert e.value.code == -1
+
+
+def test_unsupported_head_dim(api):
+    with pytest.raises(api.BaError) as e:
+        api.Plan("ttt", [0, 256], 2, 1, 96, 2, ttt_depth=3)
+    assert e.value.code == -2
+
+
+@pytest.mark.parametrize("anchors", [[5, 5, 9], [9, 5, 1], [0, 3, 64]])
+def test_bad_anchors_rejected(api, anchors):
+    with pytest.raises(api.BaError) as e:
+        api.Plan("block", [0, 64], 2, 1, 64, 2, block_size=4, anchors=anchors)
+    assert e.value.code == -1
+
+
+def test_null_and_misaligned_pointers_rejected_before_launch(api):
+    lib = api.lib()
+    p = api.Plan("ttt", [0, 64], 2, 1, 64, 2, ttt_depth=2)
+    rc = lib.ba_forward(p._h, None, None, None, None, None, None, None, None, 0, None)
+    assert rc == -1
+    rc = lib.ba_forward(p._h, *([ctypes.c_void_p(0x1001)] * 7), ctypes.c_void_p(0x1000), 1 << 30, None)
+    assert rc == -1
+    # aligned pointers but no workspace
+    rc = lib.ba_forward(p._h, *([ctypes.c_void_p(0x1000)] * 7), None, 0, None)
+    assert rc == -6
+    assert lib.ba_lse_merge(4, 96, None, None, None, None, None, None, None) == -1
