@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -21,6 +22,13 @@ int cuda_fail(cudaError_t e) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool ok_tensor(const void* p) { return p != nullptr && aligned(p, 16); }
+
+// BA_MAIN_FWD=mma selects the mma.sync main forward (kept as the measured
+// baseline of the tcgen05 kernel); anything else runs the tcgen05 kernel.
+bool use_mma_fwd() {
+  const char* v = std::getenv("BA_MAIN_FWD");
+  return v && std::strcmp(v, "mma") == 0;
+}
 
 unsigned char* ws_at(void* ws, size_t off) { return static_cast<unsigned char*>(ws) + off; }
 
@@ -239,7 +247,8 @@ int ba_forward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, c
     BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, k_b, const_cast<void*>(a.kbp), 0, st); }));
     BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, v_b, const_cast<void*>(a.vbp), 0, st); }));
   }
-  BA_TRY(timed(p, K_MAIN_FWD, st, [&] { return ba_launch_main_fwd(a, st); }));
+  BA_TRY(timed(p, K_MAIN_FWD, st,
+               [&] { return use_mma_fwd() ? ba_launch_main_fwd(a, st) : ba_launch_main_fwd_tc(a, st); }));
   if (has_b) BA_TRY(timed(p, K_BRANCH_FWD, st, [&] { return ba_launch_branch_fwd(a, st); }));
   BA_TRY(timed(p, K_MERGE, st, [&] { return ba_launch_merge_plan(a, st); }));
   return BA_OK;

@@ -30,6 +30,8 @@ struct BaBwdArgs {
 cudaError_t ba_launch_zigzag_gather(const void* src, void* dst, const int32_t* perm, int64_t outer,
                                     int64_t units, int64_t unit_bytes, int inverse, cudaStream_t st);
 // K2: causal main attention over each query tile's key segments -> O_m, l_m.
+// tcgen05 / TMEM / TMA kernel (the default) and the mma.sync kernel it replaces.
+cudaError_t ba_launch_main_fwd_tc(const BaFwdArgs& a, cudaStream_t st);
 cudaError_t ba_launch_main_fwd(const BaFwdArgs& a, cudaStream_t st);
 // K3: rank-local branch attention -> O_b, l_b.
 cudaError_t ba_launch_branch_fwd(const BaFwdArgs& a, cudaStream_t st);

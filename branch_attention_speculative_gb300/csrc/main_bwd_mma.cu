@@ -84,9 +84,11 @@ __global__ void __launch_bounds__(128, 1) main_bwd_mma_kernel(BaBwdArgs a) {
   // iteration state: (query range, query tile, stream)
   int rr = kt.qr0, ti = 0, sidx = 0;
   const int rrend = kt.qr0 + kt.nqr;
-  if (rr >= rrend) return;
-  BaQRange range = tb.bqr[rr];
-  ti = range.t0;
+  BaQRange range{0, 0, 0, 0};
+  if (rr < rrend) {
+    range = tb.bqr[rr];
+    ti = range.t0;
+  }
 
   auto load_q = [&](int tix, int sx, int buf) {
     const BaQTile qt = tb.bq[tix];
@@ -121,9 +123,10 @@ __global__ void __launch_bounds__(128, 1) main_bwd_mma_kernel(BaBwdArgs a) {
   const int posA = kt.pos0 + kA, posB = kt.pos0 + kB;
 
   int buf = 0;
-  load_q(ti, sidx, buf);
+  if (rr < rrend) load_q(ti, sidx, buf);
   cp_async_commit();
-  for (;;) {
+  // a key tile that no query sees keeps zero gradients
+  for (; rr < rrend;) {
     // next iteration
     int nrr = rr, nti = ti, nsx = sidx + 1;
     BaQRange nrange = range;
@@ -268,6 +271,7 @@ __global__ void __launch_bounds__(128, 1) main_bwd_mma_kernel(BaBwdArgs a) {
     buf ^= 1;
   }
 
+  cp_async_wait<0>();
   // epilogue: natural-order dK_m (scaled) and dV_m
   auto* dkm = static_cast<__nv_bfloat16*>(a.dkm);
   auto* dvm = static_cast<__nv_bfloat16*>(a.dvm);

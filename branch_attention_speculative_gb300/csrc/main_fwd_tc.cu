@@ -1,0 +1,386 @@
+// K2 — causal main-sequence attention forward on the 5th-generation tensor
+// cores (tcgen05, TMEM accumulators, TMA-fed 128B-swizzled tiles).
+//
+// "Online Draft Co-Training ...", ai.info summary, "Methodology in Plain
+// English": the main part is ordinary causal context-parallel attention —
+// zigzag-ring attention where K/V circulate, queries stay put, and partial
+// results are merged with the log-sum-exp rule between ring steps.  On one GPU
+// a query tile walks the key segments the planner lists for it in ring order
+// (step s: the chunks of rank (r - s) mod C below or on its own chunk); the
+// online softmax carried from one key block to the next is exactly that merge.
+//
+// One CTA = one 128-row query tile of one query stream (TTT step j, q head h)
+// against blocks of 128 keys of kv head h / G.  Warp roles:
+//   warps 0-3  softmax: thread t owns row t (TMEM lane t).  Reads S from TMEM,
+//              masks the ragged block end and the per-row causal limit on the
+//              diagonal chunk, keeps the row max / sum, writes P (bf16) into a
+//              128B-swizzled shared tile, rescales O in TMEM only when the row
+//              max grew by more than 2^8 (the values of P stay below 256), and
+//              finally writes O_m = O / l and l_m.
+//   warp 4     TMA producer: Q once, then K and V blocks into two-stage rings.
+//   warp 5     MMA issuer (one thread): S = Q K^T into one of two TMEM S
+//              buffers, then O += P V for the previous block; owns TMEM.
+// TMEM: S0 = columns [0,128), S1 = [128,256), O = [256, 256 + d).
+// Every wait is bounded (BA_WAIT_CYCLES); a timeout records BA_DEV_TIMEOUT,
+// every role leaves its loop, and TMEM is released before the CTA exits.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace {
+
+constexpr int TBM = 128;  // query rows per tile
+constexpr int TBN = 128;  // keys per block
+constexpr int NTHREADS = 192;
+
+template <int D>
+struct FwdSmem {
+  static constexpr int CB = D / 64;                       // 64-column (128-byte) blocks per row
+  static constexpr uint32_t TILE = 128u * 128u;           // one 128-row x 128-byte swizzled block
+  static constexpr uint32_t q = 0;
+  static constexpr uint32_t k = q + CB * TILE;            // [2 stages][CB blocks]
+  static constexpr uint32_t v = k + 2 * CB * TILE;        // [2 stages][CB blocks]
+  static constexpr uint32_t p = v + 2 * CB * TILE;        // [2 buffers][2 blocks of 64 keys]
+  static constexpr uint32_t bars = p + 2 * 2 * TILE;
+  static constexpr uint32_t bytes = bars + 256;
+  static constexpr uint32_t alloc = bytes + 1024;         // slack for 1024-byte alignment
+};
+
+// barrier slots (8 bytes each) after FwdSmem::bars
+enum {
+  B_QFULL = 0,
+  B_KFULL = 1,   // [2]
+  B_KEMPTY = 3,  // [2]
+  B_VFULL = 5,   // [2]
+  B_VEMPTY = 7,  // [2]
+  B_SFULL = 9,   // [2]
+  B_SEMPTY = 11, // [2]
+  B_PFULL = 13,  // [2]
+  B_ODONE = 15,  // [2]
+  B_COUNT = 17
+};
+
+struct BlockIter {
+  const BaKvSeg* seg;
+  int si, send, kb;
+  BaKvSeg cur;
+  __device__ void init(const BaKvSeg* s, int s0, int n) {
+    seg = s;
+    si = s0;
+    send = s0 + n;
+    kb = 0;
+    if (si < send) cur = seg[si];
+  }
+  __device__ bool valid() const { return si < send; }
+  __device__ void next() {
+    kb += TBN;
+    if (kb >= cur.nkeys) {
+      kb = 0;
+      ++si;
+      if (si < send) cur = seg[si];
+    }
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    main_fwd_tc_kernel(const BaFwdArgs a, const __grid_constant__ CUtensorMap tmq,
+                       const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  using L = FwdSmem<D>;
+  constexpr int CB = L::CB;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (sbase - raw);
+  const uint32_t bar0 = sbase + L::bars;
+  auto bar = [&](int i) { return bar0 + 8u * uint32_t(i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::bars + 8 * B_COUNT);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L::bars + 8 * B_COUNT + 8);
+
+  const BaShape& sh = a.sh;
+  const BaTables& tb = a.tb;
+  const int nstreams = sh.steps * sh.Hq;
+  const int si = int(blockIdx.x % nstreams);
+  const int oi = int(blockIdx.x / nstreams);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (oi >= tb.n_fq) {
+    if (tid == 0) ba_set_status(tb.status, BA_DEV_BOUNDS);
+    return;
+  }
+  // an earlier CTA already failed: leave before touching barriers or TMEM
+  if (*reinterpret_cast<volatile unsigned int*>(tb.status) != 0u) return;
+  const BaQTile tile = tb.fq[tb.forder[oi]];
+  const int kvh = si / (sh.steps * sh.G);
+  const int rem = si % (sh.steps * sh.G);
+  const int j = rem / sh.G;
+  const int h = kvh * sh.G + rem % sh.G;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(B_QFULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
+      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_SEMPTY + s), 4);
+      mbar_init(bar(B_PFULL + s), 4);
+      mbar_init(bar(B_ODONE + s), 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 256;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      mbar_expect_tx(bar(B_QFULL), CB * L::TILE);
+      for (int cb = 0; cb < CB; ++cb)
+        tma_load_3d(sbase + L::q + cb * L::TILE, &tmq, bar(B_QFULL), cb * 64, h, int(j * sh.rows + tile.row0));
+      BlockIter it;
+      it.init(tb.fseg, tile.seg0, tile.nseg);
+      for (int i = 0; it.valid(); ++i, it.next()) {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        const int key = it.cur.k0 + it.kb;
+        if (!mbar_wait(bar(B_KEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
+        mbar_expect_tx(bar(B_KFULL + st), CB * L::TILE);
+        for (int cb = 0; cb < CB; ++cb)
+          tma_load_3d(sbase + L::k + (st * CB + cb) * L::TILE, &tmk, bar(B_KFULL + st), cb * 64, kvh, key);
+        if (!mbar_wait(bar(B_VEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
+        mbar_expect_tx(bar(B_VFULL + st), CB * L::TILE);
+        for (int cb = 0; cb < CB; ++cb)
+          tma_load_3d(sbase + L::v + (st * CB + cb) * L::TILE, &tmv, bar(B_VFULL + st), cb * 64, kvh, key);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, TBN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      auto issue_pv = [&](int i) -> bool {
+        const int pb = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait(bar(B_PFULL + pb), ph, tb.status, abort_flag)) return false;
+        if (!mbar_wait(bar(B_VFULL + pb), ph, tb.status, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t pbase = sbase + L::p + pb * 2 * L::TILE;
+        const uint32_t vbase = sbase + L::v + pb * CB * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < TBN / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(pbase + (kk >> 2) * L::TILE + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, L::TILE, 1024);
+          tc_mma(tO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bar(B_ODONE + pb));
+        tc_commit(bar(B_VEMPTY + pb));
+        return true;
+      };
+      bool ok = mbar_wait(bar(B_QFULL), 0, tb.status, abort_flag);
+      BlockIter it;
+      it.init(tb.fseg, tile.seg0, tile.nseg);
+      int i = 0;
+      for (; ok && it.valid(); ++i, it.next()) {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait(bar(B_KFULL + st), ph, tb.status, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(bar(B_SEMPTY + st), ph ^ 1, tb.status, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kbase = sbase + L::k + st * CB * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
+          tc_mma(tS + st * TBN, smem_desc_sw128(sbase + L::q + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024),
+                 idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(B_SFULL + st));
+        tc_commit(bar(B_KEMPTY + st));
+        if (i > 0 && !issue_pv(i - 1)) { ok = false; break; }
+      }
+      if (ok && i > 0) issue_pv(i - 1);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (rows)
+    const int r = tid;  // TMEM lane == query row
+    const int lim = r < tile.nrows ? tb.row_lim[tile.row0 + r] : -1;
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    BlockIter it;
+    it.init(tb.fseg, tile.seg0, tile.nseg);
+    int i = 0;
+    bool ok = true;
+    for (; it.valid(); ++i, it.next()) {
+      const int sb = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      if (!mbar_wait_warp(bar(B_SFULL + sb), ph, tb.status, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      float s[TBN];
+#pragma unroll
+      for (int c = 0; c < TBN / 32; ++c) tmem_ld32(tS + lane_off + sb * TBN + c * 32, s + c * 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SEMPTY + sb));
+      // mask: ragged end of the segment, causal limit on the diagonal chunk
+      const int nvalid = it.cur.nkeys - it.kb;
+      if (it.cur.diag || nvalid < TBN) {
+        const int climit = it.cur.diag ? min(nvalid, lim - (it.cur.pos0 + it.kb) + 1) : nvalid;
+#pragma unroll
+        for (int c = 0; c < TBN; ++c)
+          if (c >= climit) s[c] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < TBN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_blk = mx * sh.scale_log2;
+      const bool grow = m_blk > m_used + 8.f;
+      const float m_next = grow ? m_blk : m_used;
+      const float base = m_next == -INFINITY ? 0.f : m_next;
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < TBN; ++c) {
+        s[c] = ex2_approx(fmaf(s[c], sh.scale_log2, -base));
+        rs += s[c];
+      }
+      // the P buffer was last read by PV(i - 2)
+      if (i >= 2 && !mbar_wait_warp(bar(B_ODONE + sb), ((i - 2) >> 1) & 1, tb.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      // rescale O (warp-uniform TMEM access) when any row's max grew
+      if (i >= 1 && __any_sync(0xffffffffu, grow)) {
+        const int pb = (i - 1) & 1;
+        if (!mbar_wait_warp(bar(B_ODONE + pb), ((i - 1) >> 1) & 1, tb.status, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const float cfac = grow ? ex2_approx(m_used - base) : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(tO + lane_off + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= cfac;
+          tmem_st32(tO + lane_off + c * 32, o);
+        }
+        tmem_wait_st();
+        l *= cfac;
+      } else if (grow) {
+        l *= ex2_approx(m_used - base);  // i == 0: O not written yet
+      }
+      m_used = m_next;
+      l += rs;
+      // P (bf16) -> swizzled K-major tile: row r, keys 8c..8c+7 in 16-byte chunk c
+      const uint32_t prow = sbase + L::p + sb * 2 * L::TILE + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+      for (int c = 0; c < TBN / 8; ++c) {
+        const uint32_t addr = prow + (c >> 3) * L::TILE + (((c & 7) ^ (r & 7)) << 4);
+        const uint32_t w0 = pack_bf16(s[8 * c + 0], s[8 * c + 1]);
+        const uint32_t w1 = pack_bf16(s[8 * c + 2], s[8 * c + 3]);
+        const uint32_t w2 = pack_bf16(s[8 * c + 4], s[8 * c + 5]);
+        const uint32_t w3 = pack_bf16(s[8 * c + 6], s[8 * c + 7]);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL + sb));
+    }
+    // epilogue: O / l and the natural-log lse of the main part
+    if (ok && i > 0 && mbar_wait_warp(bar(B_ODONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, tb.status, abort_flag)) {
+      tc_fence_after();
+      const bool write = r < tile.nrows;
+      const int64_t qrow = (int64_t(j) * sh.rows + tile.row0 + r) * sh.Hq + h;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float4* dst = reinterpret_cast<float4*>(a.om + qrow * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(tO + lane_off + c * 32, o);
+        tmem_wait_ld();
+        if (write) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[c * 8 + e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+        }
+      }
+      if (write) a.lm[qrow] = l > 0.f ? (m_used + log2f(l)) * BA_LN2 : -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+// 3-D view (d, heads, rows) of a row-major [rows][heads][d] bf16 tensor; box (64, 1, 128).
+cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows) {
+  const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
+  const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(heads) * d * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t launch(const BaFwdArgs& a, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  cudaError_t e;
+  if ((e = make_map(&mq, a.qp, D, a.sh.Hq, int64_t(a.sh.steps) * a.sh.rows)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.kmp, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.vmp, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  const int64_t grid = int64_t(a.tb.n_fq) * a.sh.steps * a.sh.Hq;
+  const int smem = int(FwdSmem<D>::alloc);
+  if ((e = cudaFuncSetAttribute(main_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+      cudaSuccess)
+    return e;
+  main_fwd_tc_kernel<D><<<unsigned(grid), NTHREADS, smem, st>>>(a, mq, mk, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t ba_launch_main_fwd_tc(const BaFwdArgs& a, cudaStream_t st) {
+  const int64_t grid = int64_t(a.tb.n_fq) * a.sh.steps * a.sh.Hq;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  return a.sh.d == 128 ? launch<128>(a, st) : launch<64>(a, st);
+}

@@ -275,8 +275,8 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
         }
       }
       kt.nqr = int32_t(p->bqr.size()) - kt.qr0;
-      if (kt.nqr > 0) p->bkv.push_back(kt);
-      else p->bqr.resize(kt.qr0);
+      // kept even when no query sees it: its dK / dV must still be written (as zeros)
+      p->bkv.push_back(kt);
     }
   }
   p->border.resize(p->bkv.size());
@@ -391,13 +391,23 @@ int ba_validate_plan(const ba_plan* p) {
   for (const BaKvTile& k : p->bkv) {
     if (k.k0 < 0 || k.nkeys < 1 || k.nkeys > BA_BWD_BN || int64_t(k.k0) + k.nkeys > T) return bad();
     if (p->tok_perm[k.k0] != k.pos0 || p->tok_perm[k.k0 + k.nkeys - 1] != k.pos0 + k.nkeys - 1) return bad();
-    if (k.qr0 < 0 || k.nqr < 1 || int64_t(k.qr0) + k.nqr > int64_t(p->bqr.size())) return bad();
+    if (k.qr0 < 0 || k.nqr < 0 || int64_t(k.qr0) + k.nqr > int64_t(p->bqr.size())) return bad();
     for (int i = 0; i < k.nqr; ++i) {
       const BaQRange& r = p->bqr[k.qr0 + i];
       if (r.t0 < 0 || r.t1 <= r.t0 || r.t1 > int64_t(p->bq.size())) return bad();
       for (int32_t q = r.t0; q < r.t1; ++q)
         if (!r.diag && p->bq[q].lim_min < k.pos0 + k.nkeys - 1) return bad();
     }
+  }
+  {
+    std::vector<char> cov(T, 0);
+    for (const BaKvTile& k : p->bkv)
+      for (int32_t i = 0; i < k.nkeys; ++i) {
+        if (cov[k.k0 + i]) return bad();
+        cov[k.k0 + i] = 1;
+      }
+    for (char c : cov)
+      if (!c) return bad();
   }
   auto is_perm = [](const std::vector<int32_t>& v, size_t n) {
     if (v.size() != n) return false;

@@ -86,35 +86,52 @@ def sample_units(wl, n, seed=1234):
     return sorted(set(picks) | set(int(x) for x in rest))
 
 
-def invariant_errors_torch(wl, t, g):
-    """The three exact gradient identities on full device gradients (fp64):
-    per kv head, sum of dK over all keys = 0, sum of dV = sum of dO over the
-    group's queries, sum <q, dq> = sum <k, dk>; each as |lhs - rhs| / sum|terms|."""
+def invariant_errors_torch(wl, t, g, chunk=1 << 18):
+    """The three exact gradient identities on full device gradients, summed
+    in fp64 over row chunks (no full-size fp64 copies): per kv head, the sum
+    of dK over all keys = 0, the sum of dV = the sum of dO over the group's
+    queries, sum <q, dq> = sum <k, dk>; each as |lhs - rhs| / sum|terms|."""
     Hkv, G, d = wl.heads_kv, wl.heads_q // wl.heads_kv, wl.head_dim
-    f = lambda x: x.double()
-    q = f(t["q_b"]).reshape(-1, wl.heads_q, d)
-    do = f(t["d_o"]).reshape(-1, wl.heads_q, d)
-    dq = f(g["dq_b"]).reshape(-1, wl.heads_q, d)
-    km, dkm, dvm = f(t["k_m"]), f(g["dk_m"]), f(g["dv_m"])
-    has_b = wl.family != "causal"
-    if has_b:
-        kb = f(t["k_b"]).reshape(-1, Hkv, d)
-        dkb = f(g["dk_b"]).reshape(-1, Hkv, d)
-        dvb = f(g["dv_b"]).reshape(-1, Hkv, d)
+    dev = t["q_b"].device
+    z = lambda *shape: torch.zeros(shape, dtype=torch.float64, device=dev)
+
+    def rows(x, heads):
+        return x.reshape(-1, heads, d)
+
+    # query side: per q head, sum_i <q_i, dq_i> and its |terms|, sum_i dO_i, sum |dO_i|
+    q, dq, do = rows(t["q_b"], wl.heads_q), rows(g["dq_b"], wl.heads_q), rows(t["d_o"], wl.heads_q)
+    qdq, qdq_abs, sdo, sdo_abs = z(wl.heads_q), z(wl.heads_q), z(wl.heads_q, d), z(wl.heads_q, d)
+    for i in range(0, q.shape[0], chunk):
+        a = (q[i:i + chunk].float() * dq[i:i + chunk].float()).sum(-1).double()
+        qdq += a.sum(0)
+        qdq_abs += a.abs().sum(0)
+        x = do[i:i + chunk].double()
+        sdo += x.sum(0)
+        sdo_abs += x.abs().sum(0)
+    # key side: per kv head, sums of dK, |dK|, dV, |dV|, <k, dk>, |<k, dk>|
+    sdk, adk, sdv, adv, kdk, kdk_abs = z(Hkv, d), z(Hkv, d), z(Hkv, d), z(Hkv, d), z(Hkv), z(Hkv)
+    pairs = [(t["k_m"], g["dk_m"], g["dv_m"])]
+    if wl.family != "causal":
+        pairs.append((t["k_b"], g["dk_b"], g["dv_b"]))
+    for k, gk, gv in pairs:
+        k, gk, gv = rows(k, Hkv), rows(gk, Hkv), rows(gv, Hkv)
+        for i in range(0, k.shape[0], chunk):
+            x, y = gk[i:i + chunk].double(), gv[i:i + chunk].double()
+            sdk += x.sum(0)
+            adk += x.abs().sum(0)
+            sdv += y.sum(0)
+            adv += y.abs().sum(0)
+            a = (k[i:i + chunk].float() * gk[i:i + chunk].float()).sum(-1).double()
+            kdk += a.sum(0)
+            kdk_abs += a.abs().sum(0)
     out = {"sum_dk": 0.0, "sum_dv": 0.0, "qdq_kdk": 0.0}
     for kh in range(Hkv):
         hs = slice(kh * G, (kh + 1) * G)
-        sdk = dkm[:, kh].sum(0) + (dkb[:, kh].sum(0) if has_b else 0)
-        adk = dkm[:, kh].abs().sum(0) + (dkb[:, kh].abs().sum(0) if has_b else 0)
-        out["sum_dk"] = max(out["sum_dk"], float((sdk.abs() / adk.clamp_min(1e-30)).max()))
-        sdv = dvm[:, kh].sum(0) + (dvb[:, kh].sum(0) if has_b else 0)
-        sdo = do[:, hs].sum((0, 1))
-        adv = dvm[:, kh].abs().sum(0) + (dvb[:, kh].abs().sum(0) if has_b else 0) + do[:, hs].abs().sum((0, 1))
-        out["sum_dv"] = max(out["sum_dv"], float(((sdv - sdo).abs() / adv.clamp_min(1e-30)).max()))
-        lt = (q[:, hs] * dq[:, hs]).sum(-1)
-        rt = (km[:, kh] * dkm[:, kh]).sum(-1)
-        rb = (kb[:, kh] * dkb[:, kh]).sum(-1) if has_b else torch.zeros(1, dtype=torch.float64, device=q.device)
-        lhs, rhs = lt.sum(), rt.sum() + rb.sum()
-        den = lt.abs().sum() + rt.abs().sum() + rb.abs().sum()
+        out["sum_dk"] = max(out["sum_dk"], float((sdk[kh].abs() / adk[kh].clamp_min(1e-30)).max()))
+        gd = sdo[hs].sum(0)
+        out["sum_dv"] = max(out["sum_dv"], float(((sdv[kh] - gd).abs() /
+                                                    (adv[kh] + sdo_abs[hs].sum(0)).clamp_min(1e-30)).max()))
+        lhs, rhs = qdq[hs].sum(), kdk[kh]
+        den = qdq_abs[hs].sum() + kdk_abs[kh]
         out["qdq_kdk"] = max(out["qdq_kdk"], float((lhs - rhs).abs() / den))
     return out
