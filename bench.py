@@ -318,7 +318,7 @@ def run_ours(args, rank, world, local):
 
     e2e = None
     if args.e2e_steps > 0:
-        e2e = run_e2e(args, plan, wl, t, info, world)
+        e2e = run_e2e(args, plan, wl, t, info, world, ws, o, lse, grads)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -366,18 +366,16 @@ def _mem_available_bytes():
     return 0
 
 
-def run_e2e(args, plan, wl, t, info, world):
+def run_e2e(args, plan, wl, t, info, world, ws, o, lse, grads):
     """Same metric through the public API with host buffers: every step
-    copies its inputs host->device from pinned memory and reads the results
-    back device->host inside the timed region."""
+    copies its inputs host->device from pinned memory (into the device input
+    buffers) and reads every result back device->host, inside the timed
+    region.  Device buffers are the ones the device-resident run used."""
     import torch
     ins = ["q_b", "k_m", "v_m", "k_b", "v_b", "d_o"]
-    outs = {"o": t["q_b"], "lse": None, "dq_b": t["q_b"], "dk_m": t["k_m"], "dv_m": t["v_m"], "dk_b": t["k_b"],
-            "dv_b": t["v_b"]}
+    outs = {"o": o, "lse": lse, **grads}
     in_bytes = sum(t[n].numel() * t[n].element_size() for n in ins)
-    lse_shape = t["q_b"].shape[:-1]
-    out_bytes = sum(v.numel() * v.element_size() for k, v in outs.items() if v is not None) + \
-        int(np.prod(lse_shape)) * 4
+    out_bytes = sum(v.numel() * v.element_size() for v in outs.values())
     need = in_bytes + out_bytes
     if _mem_available_bytes() < 1.25 * need:
         return {"value": None, "unit": UNIT, "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
@@ -385,21 +383,16 @@ def run_e2e(args, plan, wl, t, info, world):
     h_in = {n: torch.empty(t[n].shape, dtype=t[n].dtype, pin_memory=True) for n in ins}
     for n in ins:
         h_in[n].copy_(t[n])
-    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items() if v is not None}
-    h_out["lse"] = torch.empty(lse_shape, dtype=torch.float32, pin_memory=True)
-    d_in = {n: torch.empty_like(t[n]) for n in ins}
-    ws = plan.workspace()
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
 
     def e2e_step():
         for n in ins:
-            d_in[n].copy_(h_in[n], non_blocking=True)
-        o, lse = plan.forward(d_in["q_b"], d_in["k_m"], d_in["v_m"], d_in["k_b"], d_in["v_b"], workspace=ws)
-        g = plan.backward(d_in["q_b"], d_in["k_m"], d_in["v_m"], d_in["k_b"], d_in["v_b"], o, lse, d_in["d_o"],
-                          workspace=ws)
-        h_out["o"].copy_(o, non_blocking=True)
-        h_out["lse"].copy_(lse, non_blocking=True)
-        for k in ("dq_b", "dk_m", "dv_m", "dk_b", "dv_b"):
-            h_out[k].copy_(g[k], non_blocking=True)
+            t[n].copy_(h_in[n], non_blocking=True)
+        plan.forward(t["q_b"], t["k_m"], t["v_m"], t["k_b"], t["v_b"], o=o, lse=lse, workspace=ws)
+        plan.backward(t["q_b"], t["k_m"], t["v_m"], t["k_b"], t["v_b"], o, lse, t["d_o"], grads=grads,
+                      workspace=ws)
+        for k, v in outs.items():
+            h_out[k].copy_(v, non_blocking=True)
         torch.cuda.synchronize()
 
     e2e_step()

@@ -30,6 +30,12 @@ bool use_mma_fwd() {
   return v && std::strcmp(v, "mma") == 0;
 }
 
+// Same for the backward (BA_MAIN_BWD=mma); head_dim 64 always takes mma.sync.
+bool use_mma_bwd(const BaShape& sh) {
+  const char* v = std::getenv("BA_MAIN_BWD");
+  return (v && std::strcmp(v, "mma") == 0) || !ba_main_bwd_tc_supported(sh);
+}
+
 unsigned char* ws_at(void* ws, size_t off) { return static_cast<unsigned char*>(ws) + off; }
 
 int check_ws(const ba_plan* p, void* ws, size_t bytes) {
@@ -296,7 +302,9 @@ int ba_backward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, 
     BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, v_b, const_cast<void*>(a.vbp), 0, st); }));
   }
   BA_TRY(timed(p, K_BWD_PREP, st, [&] { return ba_launch_bwd_prep(a, st); }));
-  BA_TRY(timed(p, K_MAIN_BWD, st, [&] { return ba_launch_main_bwd(a, st); }));
+  BA_TRY(timed(p, K_MAIN_BWD, st, [&] {
+    return use_mma_bwd(a.sh) ? ba_launch_main_bwd(a, st) : ba_launch_main_bwd_tc(a, st);
+  }));
   BA_TRY(timed(p, K_BRANCH_BWD, st, [&] { return ba_launch_branch_bwd(a, st); }));
   return BA_OK;
 }

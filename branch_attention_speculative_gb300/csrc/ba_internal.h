@@ -10,7 +10,7 @@
 #define BA_FWD_BM 128   // query rows per forward tile
 #define BA_FWD_BN 64    // keys per forward key block (work estimate only)
 #define BA_BWD_BM 64    // query rows per backward query tile
-#define BA_BWD_BN 64    // keys per backward key tile
+#define BA_BWD_BN 128   // keys per backward key tile
 
 // Device status word values (first word of the workspace).
 #define BA_DEV_OK 0u

@@ -177,8 +177,9 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
       load_row<D>(dop + qrow * D, lane, go);
 #pragma unroll
       for (int e = 0; e < E; ++e) gq[e] = a.dqacc[qrow * D + lane * E + e];
-      const float l2 = a.lsep[qrow] * BA_LOG2E;
-      const float delta = a.dlt[qrow];
+      const int64_t srow = (j * sh.Hq + kvh * sh.G + g) * sh.rows + r;  // stream-major
+      const float l2 = a.lsep[srow] * BA_LOG2E;
+      const float delta = a.dlt[srow];
       const int nk = keys_of_query(sh, qi);
       for (int i = 0; i < nk; ++i) {
         float dot = 0.f, dpv = 0.f;

@@ -3,17 +3,18 @@
 //
 // "Online Draft Co-Training ...", rainbus page, method step 5 and core method:
 // the backward replays the same ring and accumulates gradients locally.  On
-// one GPU a key tile (64 keys of one kv head, inside one zigzag chunk) meets
+// one GPU a key tile (128 keys of one kv head, inside one zigzag chunk) meets
 // the query tiles of rank (r + s) mod C at replay step s, in the order the
 // planner lists them, for every query stream (step j, q head) of its group.
 // P is recomputed from the merged lse: the merged result is the single softmax
 // over main and branch keys, so P_ij = exp(scale q_i.k_j - l_i) is already the
 // full-softmax probability and dS = P * (dP - Delta) splits by key set.
 //
-// CTA: 4 warps, warp w owns keys 16w..16w+15: it computes S^T and dP^T for
-// its keys against a 64-row query tile, accumulates dV and dK in registers,
-// and writes its dS^T to shared memory; then each warp forms 16 rows of
-// dQ = dS K and adds them (scaled) into the fp32 dQ accumulator with atomics.
+// CTA: 8 warps over a 128-key tile, warp w owns keys 16w..16w+15: it computes
+// S^T and dP^T for its keys against a 64-row query tile, accumulates dV and dK
+// in registers, and writes its dS^T to shared memory; then each warp forms 16
+// rows x d/2 columns of dQ = dS K and adds them (scaled) into the fp32 dQ
+// accumulator with atomics.
 // Query/dO tiles are double-buffered with cp.async.
 #include <math.h>
 
@@ -22,8 +23,9 @@
 
 namespace {
 
-constexpr int QB = 64;  // queries per tile (BA_BWD_BM)
-constexpr int KB = 64;  // keys per tile (BA_BWD_BN)
+constexpr int QB = 64;   // queries per tile (BA_BWD_BM)
+constexpr int KB = 128;  // keys per tile (BA_BWD_BN)
+constexpr int NT = 256;  // 8 warps, 16 keys each
 
 template <int D>
 struct BwdSmem {
@@ -41,7 +43,7 @@ struct BwdSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(128, 1) main_bwd_mma_kernel(BaBwdArgs a) {
+__global__ void __launch_bounds__(NT, 1) main_bwd_mma_kernel(BaBwdArgs a) {
   using L = BwdSmem<D>;
   constexpr int LD = L::LD, LDS = L::LDS, CH = D / 8;
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(128, 1) main_bwd_mma_kernel(BaBwdArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
 
-  for (int c = tid; c < KB * CH; c += 128) {
+  for (int c = tid; c < KB * CH; c += NT) {
     const int r = c / CH, col = (c % CH) * 8;
     const bool ok = r < kt.nkeys;
     const int64_t key = int64_t(kt.k0) + (ok ? r : 0);
@@ -96,18 +98,18 @@ __global__ void __launch_bounds__(128, 1) main_bwd_mma_kernel(BaBwdArgs a) {
     const int64_t base = (int64_t(j) * sh.rows * sh.Hq + h) * D;
     __nv_bfloat16* qd = Qs + buf * QB * LD;
     __nv_bfloat16* gd = Gs + buf * QB * LD;
-    for (int c = tid; c < QB * CH; c += 128) {
+    for (int c = tid; c < QB * CH; c += NT) {
       const int r = c / CH, col = (c % CH) * 8;
       const bool ok = r < qt.nrows;
       const int64_t off = base + int64_t(qt.row0 + (ok ? r : 0)) * qstride + col;
       cp_async16(smem_u32(qd + r * LD + col), qp + off, ok ? 16 : 0);
       cp_async16(smem_u32(gd + r * LD + col), dop + off, ok ? 16 : 0);
     }
-    for (int r = tid; r < QB; r += 128) {
+    for (int r = tid; r < QB; r += NT) {
       const bool ok = r < qt.nrows;
-      const int64_t qrow = (int64_t(j) * sh.rows + qt.row0 + (ok ? r : 0)) * sh.Hq + h;
-      L2s[buf * QB + r] = ok ? a.lsep[qrow] * BA_LOG2E : INFINITY;
-      Dls[buf * QB + r] = ok ? a.dlt[qrow] : 0.f;
+      const int64_t srow = (int64_t(j) * sh.Hq + h) * sh.rows + qt.row0 + (ok ? r : 0);
+      L2s[buf * QB + r] = ok ? a.lsep[srow] * BA_LOG2E : INFINITY;
+      Dls[buf * QB + r] = ok ? a.dlt[srow] : 0.f;
       Lims[buf * QB + r] = ok ? tb.row_lim[qt.row0 + r] : -1;
     }
   };
@@ -225,19 +227,19 @@ __global__ void __launch_bounds__(128, 1) main_bwd_mma_kernel(BaBwdArgs a) {
       *reinterpret_cast<uint32_t*>(Ss + kB * LDS + q) = pack_bf16(dpt[nt][2], dpt[nt][3]);
     }
     __syncthreads();
-    // dQ rows 16w..16w+15 = dS K, in two halves of d
-    const int qA = warp * 16 + g, qB = qA + 8;
+    // dQ = dS K: warp w takes query rows 16(w % 4).. and d-half w / 4
+    const int qw = warp & 3, half = warp >> 2;
+    const int qA = qw * 16 + g, qB = qA + 8;
     const int64_t rowA = (int64_t(j) * sh.rows + qt.row0 + qA) * sh.Hq + h;
     const int64_t rowB = (int64_t(j) * sh.rows + qt.row0 + qB) * sh.Hq + h;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    {
       float dq[D / 16][4];
 #pragma unroll
       for (int i = 0; i < D / 16; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
 #pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
+      for (int kq = 0; kq < KB / 16; ++kq) {
         uint32_t aa[4];
-        ldsm_x4_t(smem_u32(Ss + (kq * 16 + (lane & 7) + (lane >> 4) * 8) * LDS + warp * 16 + ((lane >> 3) & 1) * 8),
+        ldsm_x4_t(smem_u32(Ss + (kq * 16 + (lane & 7) + (lane >> 4) * 8) * LDS + qw * 16 + ((lane >> 3) & 1) * 8),
                   aa[0], aa[1], aa[2], aa[3]);
 #pragma unroll
         for (int dp = 0; dp < D / 32; ++dp) {
@@ -303,11 +305,11 @@ cudaError_t ba_launch_main_bwd(const BaBwdArgs& a, cudaStream_t st) {
   if (a.sh.d == 128) {
     const int smem = int(BwdSmem<128>::bytes);
     cudaFuncSetAttribute(main_bwd_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    main_bwd_mma_kernel<128><<<unsigned(grid), 128, smem, st>>>(a);
+    main_bwd_mma_kernel<128><<<unsigned(grid), NT, smem, st>>>(a);
   } else {
     const int smem = int(BwdSmem<64>::bytes);
     cudaFuncSetAttribute(main_bwd_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    main_bwd_mma_kernel<64><<<unsigned(grid), 128, smem, st>>>(a);
+    main_bwd_mma_kernel<64><<<unsigned(grid), NT, smem, st>>>(a);
   }
   return cudaGetLastError();
 }
