@@ -126,13 +126,24 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Largest value over the ranks (timings: the job is as slow as its slowest
+    replica).  Uses a CUDA tensor under NCCL and a CPU tensor under gloo."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_throughput(ms_local: float, flops_per_replica: float, world: int):
+    """Whole-job throughput of ``world`` independent replicas (weak scaling):
+    every rank runs the full workload, the step time is the max over ranks.
+    Returns (TFLOP/s over all ranks, ms per step)."""
+    ms = max_over_ranks(ms_local, world)
+    return world * flops_per_replica / (ms / 1e3) / 1e12, ms
 
 
 # --------------------------------------------------------------------------- oracle sample (CPU)
@@ -278,14 +289,13 @@ def run_ours(args, rank, world, local):
     clocks = sampler.stop()
     kt = plan.profile_read()
     plan.profile(False)
-    ms = e0.elapsed_time(e1) / args.steps
-    ms = max_over_ranks(ms, world)
+    ms_local = e0.elapsed_time(e1) / args.steps
     status = plan.check_device_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {status} after timed steps")
 
     flops = info["fwd_flops"] + info["bwd_flops"]
-    value = world * flops / (ms / 1e3) / 1e12
+    value, ms = aggregate_throughput(ms_local, flops, world)
     peak_t = peaks["bf16_tflops_sustained"]
 
     kernels = {}

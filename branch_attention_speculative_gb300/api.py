@@ -90,6 +90,7 @@ _SIGS = {
     "ba_check_device_status": (ctypes.c_int, [_P, _P, _P]),
     "ba_zigzag_pack": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "ba_lse_merge": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P]),
+    "ba_selftest_wait_timeout": (ctypes.c_int, [_P, _P, ctypes.c_size_t, ctypes.c_int64, _P]),
     "ba_profile_enable": (ctypes.c_int, [_P, ctypes.c_int32]),
     "ba_profile_read": (ctypes.c_int, [_P, ctypes.POINTER(_KTime), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "ba_last_cuda_error": (ctypes.c_char_p, []),
@@ -292,6 +293,11 @@ class Plan:
         n = ctypes.c_int32()
         _check(lib().ba_profile_read(self._h, buf, 16, ctypes.byref(n)), "ba_profile_read")
         return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n.value)}
+
+    def selftest_wait_timeout(self, workspace, cycles: int, stream=None):
+        """Runs the bounded-wait failure self-test (see include/ba.h)."""
+        _check(lib().ba_selftest_wait_timeout(self._h, _ptr(workspace), workspace.numel(), int(cycles),
+                                              _stream(stream)), "ba_selftest_wait_timeout")
 
     def check_device_status(self, workspace, stream=None) -> int:
         return int(lib().ba_check_device_status(self._h, _ptr(workspace), _stream(stream)))

@@ -334,6 +334,16 @@ int ba_zigzag_pack(ba_plan_t p, int32_t role, const void* src, void* dst, int32_
   return BA_OK;
 }
 
+int ba_selftest_wait_timeout(ba_plan_t p, void* workspace, size_t workspace_bytes, int64_t cycles, void* stream) {
+  if (!p || cycles < 0 || cycles > (int64_t(1) << 32)) return BA_ERR_INVALID_ARG;
+  if (int rc = check_ws(p, workspace, workspace_bytes)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  BA_TRY(cudaMemsetAsync(ws_at(workspace, p->ws.status), 0, 256, st));
+  BA_TRY(ba_launch_selftest_wait_timeout(reinterpret_cast<unsigned int*>(ws_at(workspace, p->ws.status)),
+                                         static_cast<long long>(cycles), st));
+  return BA_OK;
+}
+
 int ba_lse_merge(int64_t rows, int32_t head_dim, const float* o_m, const float* l_m, const float* o_b,
                  const float* l_b, void* o, float* l, void* stream) {
   if (rows < 0 || (head_dim != 64 && head_dim != 128)) return BA_ERR_INVALID_ARG;

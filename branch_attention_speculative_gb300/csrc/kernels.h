@@ -50,3 +50,6 @@ cudaError_t ba_launch_main_bwd_tc(const BaBwdArgs& a, cudaStream_t st);
 cudaError_t ba_launch_main_bwd(const BaBwdArgs& a, cudaStream_t st);
 // K7 (+K8): branch backward: dK_b, dV_b (natural); dQ = accumulator + branch part -> natural bf16.
 cudaError_t ba_launch_branch_bwd(const BaBwdArgs& a, cudaStream_t st);
+
+// Self-test: a bounded wait on a barrier nothing completes (records BA_DEV_TIMEOUT).
+cudaError_t ba_launch_selftest_wait_timeout(unsigned int* status, long long cycles, cudaStream_t st);

@@ -48,8 +48,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits for the phase of `bar` with the given parity.  Returns false (and
 // records a timeout in *status) if it does not complete within
 // BA_WAIT_CYCLES, or at once if *abort is already set.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* status,
-                                          volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* status, volatile int* abort,
+                                          long long limit = BA_WAIT_CYCLES) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t n = 0;; ++n) {
@@ -59,7 +59,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
       *abort = 1;
       return false;
     }
-    if (clock64() - t0 > BA_WAIT_CYCLES) {
+    if (clock64() - t0 > limit) {
       ba_set_status(status, BA_DEV_TIMEOUT);
       *abort = 1;
       return false;

@@ -180,6 +180,15 @@ int ba_check_device_status(ba_plan_t plan, void* workspace, void* stream);
 int ba_zigzag_pack(ba_plan_t plan, int32_t role, const void* src, void* dst, int32_t inverse,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Failure-path self-test (no counterpart on the pages): launches one CTA
+ * that waits, with the library's bounded mbarrier wait, on a barrier that
+ * nothing completes.  After `cycles` SM clocks (at most 2^32) the wait gives
+ * up, records a timeout in the workspace status word and the kernel returns;
+ * ba_check_device_status then reports BA_ERR_DEVICE_TIMEOUT.  Nothing traps,
+ * faults or spins without bound. */
+int ba_selftest_wait_timeout(ba_plan_t plan, void* workspace, size_t workspace_bytes, int64_t cycles,
+                             void* stream);
+
 /* Eq. 2 on caller buffers, row by row, no permutation (rainbus page, core
  * method, Eq. 2):  l = log(e^l_m + e^l_b),
  *   o = (e^(l_m-l) o_m + e^(l_b-l) o_b) / (e^(l_m-l) + e^(l_b-l)).
