@@ -91,6 +91,7 @@ _SIGS = {
     "ba_zigzag_pack": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "ba_lse_merge": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "ba_selftest_wait_timeout": (ctypes.c_int, [_P, _P, ctypes.c_size_t, ctypes.c_int64, _P]),
+    "ba_forward_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ba_profile_enable": (ctypes.c_int, [_P, ctypes.c_int32]),
     "ba_profile_read": (ctypes.c_int, [_P, ctypes.POINTER(_KTime), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "ba_last_cuda_error": (ctypes.c_char_p, []),
@@ -258,6 +259,22 @@ class Plan:
         rc = lib().ba_forward(self._h, _ptr(q_b), _ptr(k_m), _ptr(v_m), _ptr(k_b), _ptr(v_b), _ptr(o), _ptr(lse),
                               _ptr(workspace), workspace.numel(), _stream(stream))
         _check(rc, "ba_forward")
+        return o, lse
+
+    def forward_noalloc(self, q_b, k_m, v_m, k_b=None, v_b=None, o=None, lse=None, stream=None):
+        """Forward through ba_forward_noalloc: the library's static scratch array
+        replaces the workspace (plans up to 64 MiB of workspace).  Outputs must
+        be given or are allocated here, by the caller side, before the call."""
+        self._check_inputs(q_b, k_m, v_m, k_b, v_b)
+        if o is None:
+            o = torch.empty_like(q_b)
+        if lse is None:
+            lse = torch.empty(q_b.shape[:-1], dtype=torch.float32, device=q_b.device)
+        _want(o, self.q_shape(), torch.bfloat16, "o")
+        _want(lse, self.q_shape()[:-1], torch.float32, "lse")
+        rc = lib().ba_forward_noalloc(self._h, _ptr(q_b), _ptr(k_m), _ptr(v_m), _ptr(k_b), _ptr(v_b), _ptr(o),
+                                      _ptr(lse), _stream(stream))
+        _check(rc, "ba_forward_noalloc")
         return o, lse
 
     def backward(self, q_b, k_m, v_m, k_b, v_b, o, lse, d_o, grads=None, workspace=None, stream=None):

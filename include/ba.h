@@ -180,6 +180,24 @@ int ba_check_device_status(ba_plan_t plan, void* workspace, void* stream);
 int ba_zigzag_pack(ba_plan_t plan, int32_t role, const void* src, void* dst, int32_t inverse,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Forward pass that allocates nothing (no counterpart on the pages).
+ * For callers that cannot allocate device memory where they run attention,
+ * e.g. a plugin called from another framework's execution loop, where a
+ * cudaMalloc would break that framework's memory plan or stall its stream.
+ * Same inputs, outputs and results as ba_forward, but the workspace is one
+ * file-scope device array of BA_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU
+ * loading this library holds until the process exits.  Plans whose
+ * ba_workspace_bytes exceeds that limit are rejected with BA_ERR_WORKSPACE
+ * before anything runs.  The first call on a device looks the array's device
+ * address up (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls share the array and it keeps the
+ * last call's contents (what must start at zero is cleared by each call);
+ * calls that overlap on the GPU race on it, so order them.  No cudaMalloc,
+ * cudaFree or other allocating routine is called. */
+#define BA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int ba_forward_noalloc(ba_plan_t plan, const void* q_b, const void* k_m, const void* v_m, const void* k_b,
+                       const void* v_b, void* o, float* lse, void* stream);
+
 /* Failure-path self-test (no counterpart on the pages): launches one CTA
  * that waits, with the library's bounded mbarrier wait, on a barrier that
  * nothing completes.  After `cycles` SM clocks (at most 2^32) the wait gives
