@@ -222,6 +222,12 @@ def host_cores():
 # --------------------------------------------------------------------------- our arm
 
 
+# GEMMs per (row, key) pair each main-attention kernel runs: forward S and PV;
+# fused backward (mma.sync) S, dP, dV, dK, dQ; split backward: key-stationary
+# S, dP, dV, dK and query-stationary S, dP, dQ.
+MAIN_KERNEL_GEMMS = {"main_fwd": 2, "main_bwd": 5, "main_bwd_kv": 4, "main_bwd_dq": 3}
+
+
 def kernel_bytes(wl, info, name):
     """Algorithmic HBM bytes per step of a memory-bound kernel."""
     R = info["query_rows"]
@@ -247,6 +253,8 @@ def run_ours(args, rank, world, local):
 
     peaks = load_peaks()
     wl = W.config(args.config)
+    if args.tokens:
+        wl = resize_workload(wl, args.tokens)
     plan = api.Plan.from_workload(wl)
     info = plan.info()
     t = W.make_tensors(wl, device="cuda")
@@ -302,8 +310,12 @@ def run_ours(args, rank, world, local):
     for name, (n, tot) in kt.items():
         per = tot / max(n, 1)
         ent = {"launches": n, "ms_total_per_step": tot / args.steps, "ms_per_launch": per}
-        if name in ("main_fwd", "main_bwd"):
-            f = 4.0 * wl.head_dim * info["main_pairs"] * (1.0 if name == "main_fwd" else 2.5)
+        gemms = MAIN_KERNEL_GEMMS.get(name)
+        if gemms is not None:
+            # algorithmic flops of the GEMMs the kernel must run: 2 d flops per
+            # (row, key) pair per GEMM (S, P V, dP, dV, dK, dQ, ...)
+            f = 2.0 * wl.head_dim * info["main_pairs"] * gemms
+            ent["gemms_per_pair"] = gemms
             ent["achieved"] = f / (tot / args.steps / 1e3) / 1e12
             ent["unit"] = "TFLOP/s"
         else:
@@ -314,7 +326,7 @@ def run_ours(args, rank, world, local):
         kernels[name] = ent
     dom = max(kt.items(), key=lambda kv: kv[1][1])[0] if kt else None
     roofline = None
-    if dom is not None:
+    if dom is not None and "achieved" in kernels[dom]:
         e = kernels[dom]
         if e.get("unit") == "TFLOP/s":
             roofline = {"kernel": dom, "bound": "tensor", "achieved": e["achieved"], "peak": peak_t,
@@ -364,6 +376,22 @@ def run_ours(args, rank, world, local):
         "cpu_baseline": cpu,
     }
     return line
+
+
+def resize_workload(wl, tokens: int):
+    """The same shape with one main sequence of ``tokens`` tokens (a multiple
+    of 2C); block families keep their anchor density.  Used for profiling
+    captures that must stay small."""
+    from branch_attention_speculative_gb300 import workloads as W
+    if tokens % (2 * wl.cp) != 0:
+        raise SystemExit(f"--tokens must be a multiple of 2C = {2 * wl.cp}")
+    cu = W.cu_from_lens([tokens])
+    anchors = None
+    if wl.family == "block":
+        per = max(1, int(round(wl.anchors_per_seq * tokens / (wl.tokens / wl.num_seqs))))
+        anchors = W.sample_anchors(np.random.default_rng(wl.seed), cu, per)
+    return W.Workload(f"{wl.name}_T{tokens}", wl.family, cu, wl.heads_q, wl.heads_kv, wl.head_dim, wl.cp,
+                      wl.depth, wl.block, anchors, wl.seed)
 
 
 def _mem_available_bytes():
@@ -468,6 +496,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling only: shrink the main sequence to this many tokens")
     args = ap.parse_args()
 
     rank, world, local = dist_setup()

@@ -108,9 +108,11 @@ cudaError_t pack(const ba_plan* p, const BaTables& tb, int role, const void* src
     if (e_ != cudaSuccess) return cuda_fail(e_); \
   } while (0)
 
-enum KernelId { K_PACK = 0, K_MAIN_FWD, K_BRANCH_FWD, K_MERGE, K_BWD_PREP, K_MAIN_BWD, K_BRANCH_BWD, K_COUNT };
-const char* const kKernelNames[K_COUNT] = {"zigzag_pack", "main_fwd", "branch_fwd", "lse_merge",
-                                           "bwd_prep",    "main_bwd", "branch_bwd"};
+enum KernelId {
+  K_PACK = 0, K_MAIN_FWD, K_BRANCH_FWD, K_MERGE, K_BWD_PREP, K_MAIN_BWD, K_MAIN_BWD_DQ, K_BRANCH_BWD, K_COUNT
+};
+const char* const kKernelNames[K_COUNT] = {"zigzag_pack", "main_fwd",    "branch_fwd", "lse_merge",
+                                           "bwd_prep",    "main_bwd_kv", "main_bwd_dq", "branch_bwd"};
 
 // Records an event pair around one launch when profiling is on.
 template <class F>
@@ -286,8 +288,7 @@ int ba_backward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, 
   a.d_o = d_o;
   a.lse = lse;
   a.dop = ws_at(workspace, w.dop);
-  a.dlt = reinterpret_cast<float*>(ws_at(workspace, w.dlt));
-  a.lsep = reinterpret_cast<float*>(ws_at(workspace, w.lsep));
+  a.rowrec = reinterpret_cast<float4*>(ws_at(workspace, w.rowrec));
   a.dqacc = reinterpret_cast<float*>(ws_at(workspace, w.dqacc));
   a.dq = dq_b;
   a.dkm = dk_m;
@@ -302,9 +303,12 @@ int ba_backward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, 
     BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, v_b, const_cast<void*>(a.vbp), 0, st); }));
   }
   BA_TRY(timed(p, K_BWD_PREP, st, [&] { return ba_launch_bwd_prep(a, st); }));
-  BA_TRY(timed(p, K_MAIN_BWD, st, [&] {
-    return use_mma_bwd(a.sh) ? ba_launch_main_bwd(a, st) : ba_launch_main_bwd_tc(a, st);
-  }));
+  if (use_mma_bwd(a.sh)) {
+    BA_TRY(timed(p, K_MAIN_BWD, st, [&] { return ba_launch_main_bwd(a, st); }));
+  } else {
+    BA_TRY(timed(p, K_MAIN_BWD, st, [&] { return ba_launch_main_bwd_kv_tc(a, st); }));
+    BA_TRY(timed(p, K_MAIN_BWD_DQ, st, [&] { return ba_launch_main_bwd_q_tc(a, st); }));
+  }
   BA_TRY(timed(p, K_BRANCH_BWD, st, [&] { return ba_launch_branch_bwd(a, st); }));
   return BA_OK;
 }

@@ -178,8 +178,9 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
 #pragma unroll
       for (int e = 0; e < E; ++e) gq[e] = a.dqacc[qrow * D + lane * E + e];
       const int64_t srow = (j * sh.Hq + kvh * sh.G + g) * sh.rows + r;  // stream-major
-      const float l2 = a.lsep[srow] * BA_LOG2E;
-      const float delta = a.dlt[srow];
+      const float4 rec = a.rowrec[srow];
+      const float l2 = rec.x;
+      const float delta = rec.y;
       const int nk = keys_of_query(sh, qi);
       for (int i = 0; i < nk; ++i) {
         float dot = 0.f, dpv = 0.f;

@@ -22,7 +22,7 @@ struct BaBwdArgs {
   const void *o, *d_o;                     // natural (bf16)
   const float* lse;                        // natural (fp32)
   void* dop;                               // packed dO (bf16)
-  float *dlt, *lsep;                       // packed Delta, lse (fp32, [step][head][row])
+  float4* rowrec;                          // per (step, head, row), stream-major: {lse*log2e, Delta, limit, 0}
   float* dqacc;                            // packed dQ accumulator (fp32, like q_b)
   void *dq, *dkm, *dvm, *dkb, *dvb;        // natural gradients (bf16)
 };
@@ -44,9 +44,11 @@ cudaError_t ba_launch_merge_rows(int64_t rows, int d, const float* om, const flo
 // K5: Delta = rowsum(dO * O), pack dO / lse, zero the dQ accumulator.
 cudaError_t ba_launch_bwd_prep(const BaBwdArgs& a, cudaStream_t st);
 // K6: main-attention backward (key-stationary): dK_m, dV_m (natural), dQ into the accumulator.
-// tcgen05 kernel (head_dim 128) and the mma.sync kernel (any head_dim; the baseline).
+// tcgen05 path (head_dim 128): key-stationary dK/dV kernel + query-stationary dQ
+// kernel; and the mma.sync kernel (any head_dim; the baseline, dQ by atomics).
 bool ba_main_bwd_tc_supported(const BaShape& sh);
-cudaError_t ba_launch_main_bwd_tc(const BaBwdArgs& a, cudaStream_t st);
+cudaError_t ba_launch_main_bwd_kv_tc(const BaBwdArgs& a, cudaStream_t st);
+cudaError_t ba_launch_main_bwd_q_tc(const BaBwdArgs& a, cudaStream_t st);
 cudaError_t ba_launch_main_bwd(const BaBwdArgs& a, cudaStream_t st);
 // K7 (+K8): branch backward: dK_b, dV_b (natural); dQ = accumulator + branch part -> natural bf16.
 cudaError_t ba_launch_branch_bwd(const BaBwdArgs& a, cudaStream_t st);

@@ -108,8 +108,9 @@ __global__ void __launch_bounds__(NT, 1) main_bwd_mma_kernel(BaBwdArgs a) {
     for (int r = tid; r < QB; r += NT) {
       const bool ok = r < qt.nrows;
       const int64_t srow = (int64_t(j) * sh.Hq + h) * sh.rows + qt.row0 + (ok ? r : 0);
-      L2s[buf * QB + r] = ok ? a.lsep[srow] * BA_LOG2E : INFINITY;
-      Dls[buf * QB + r] = ok ? a.dlt[srow] : 0.f;
+      const float4 rec = a.rowrec[srow];
+      L2s[buf * QB + r] = ok ? rec.x : INFINITY;
+      Dls[buf * QB + r] = ok ? rec.y : 0.f;
       Lims[buf * QB + r] = ok ? tb.row_lim[qt.row0 + r] : -1;
     }
   };

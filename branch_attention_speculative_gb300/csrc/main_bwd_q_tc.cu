@@ -1,0 +1,360 @@
+// K6 (dQ part) — gradient of the main-sequence queries on the tcgen05 tensor
+// cores, query-stationary.
+//
+// "Online Draft Co-Training ...", rainbus page, method step 5: the backward
+// replays the ring.  For dQ the replay has the forward's shape: one CTA keeps a
+// 128-row query tile of one query stream (TTT step j, q head h) and walks the
+// key segments the planner lists for it in ring order.  P is recomputed from
+// the merged lse (exact for both key sets, since the merged result is the
+// single softmax over their union), so no running max is needed:
+//   S  = Q K^T          M=128 queries, N=128 keys, K=d        -> TMEM (2 buffers)
+//   dP = dO V^T         same                                  -> TMEM
+//   (threads)  P = exp2(S * scale*log2e - lse*log2e) with the causal / ragged
+//              mask, dS = P (dP - Delta), written as bf16 into a 128B-swizzled
+//              shared tile [query][key]
+//   dQ += dS K          M=128 queries, N=d, K=128 keys (K read MN-major) -> TMEM
+// dQ stays in TMEM for the whole tile and is written once, scaled, into the
+// fp32 dQ accumulator (no atomics, no read-modify-write); the branch backward
+// adds the branch part and writes the bf16 result.
+// TMEM: S0 [0,128), S1 [128,256), dP [256,384), dQ [384,512).
+// Warps: 0-3 compute (thread = query row = TMEM lane), 4 TMA, 5 MMA + TMEM.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace {
+
+constexpr int QBM = 128;  // query rows per tile (BA_FWD_BM)
+constexpr int KBN = 128;  // keys per block
+constexpr int NTHREADS = 192;
+
+struct DqSmem {
+  static constexpr uint32_t TILE = 128u * 128u;  // [128 rows][64 columns] bf16, swizzled
+  static constexpr uint32_t q = 0;               // 2 blocks
+  static constexpr uint32_t go = q + 2 * TILE;   // 2 blocks
+  static constexpr uint32_t k = go + 2 * TILE;   // [2 stages][2 blocks]
+  static constexpr uint32_t v = k + 4 * TILE;    // [2 stages][2 blocks]
+  static constexpr uint32_t ds = v + 4 * TILE;   // dS [128 queries][128 keys]: 2 blocks
+  static constexpr uint32_t bars = ds + 2 * TILE;
+  static constexpr uint32_t bytes = bars + 256;
+  static constexpr uint32_t alloc = bytes + 1024;
+};
+
+enum {
+  B_QFULL = 0,
+  B_KFULL = 1,    // [2]
+  B_KEMPTY = 3,   // [2]
+  B_VFULL = 5,    // [2]
+  B_VEMPTY = 7,   // [2]
+  B_SFULL = 9,    // [2]
+  B_SEMPTY = 11,  // [2]
+  B_DPFULL = 13,
+  B_DPEMPTY = 14,
+  B_DSFULL = 15,
+  B_DSEMPTY = 16,
+  B_COUNT = 17
+};
+
+struct BlockIter {
+  const BaKvSeg* seg;
+  int si, send, kb;
+  BaKvSeg cur;
+  __device__ void init(const BaKvSeg* s, int s0, int n) {
+    seg = s;
+    si = s0;
+    send = s0 + n;
+    kb = 0;
+    if (si < send) cur = seg[si];
+  }
+  __device__ bool valid() const { return si < send; }
+  __device__ void next() {
+    kb += KBN;
+    if (kb >= cur.nkeys) {
+      kb = 0;
+      ++si;
+      if (si < send) cur = seg[si];
+    }
+  }
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    main_bwd_q_tc_kernel(const BaBwdArgs a, const __grid_constant__ CUtensorMap tmq,
+                         const __grid_constant__ CUtensorMap tmdo, const __grid_constant__ CUtensorMap tmk,
+                         const __grid_constant__ CUtensorMap tmv) {
+  using L = DqSmem;
+  constexpr int D = 128;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (sbase - raw);
+  const uint32_t bar0 = sbase + L::bars;
+  auto bar = [&](int i) { return bar0 + 8u * uint32_t(i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::bars + 8 * B_COUNT);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L::bars + 8 * B_COUNT + 8);
+
+  const BaShape& sh = a.sh;
+  const BaTables& tb = a.tb;
+  const int nstreams = sh.steps * sh.Hq;
+  const int si = int(blockIdx.x % nstreams);
+  const int oi = int(blockIdx.x / nstreams);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (oi >= tb.n_fq) {
+    if (tid == 0) ba_set_status(tb.status, BA_DEV_BOUNDS);
+    return;
+  }
+  if (*reinterpret_cast<volatile unsigned int*>(tb.status) != 0u) return;
+  const BaQTile tile = tb.fq[tb.forder[oi]];
+  const int kvh = si / (sh.steps * sh.G);
+  const int rem = si % (sh.steps * sh.G);
+  const int j = rem / sh.G;
+  const int h = kvh * sh.G + rem % sh.G;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(B_QFULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
+      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_SEMPTY + s), 4);
+    }
+    mbar_init(bar(B_DPFULL), 1);
+    mbar_init(bar(B_DPEMPTY), 4);
+    mbar_init(bar(B_DSFULL), 4);
+    mbar_init(bar(B_DSEMPTY), 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tDP = tmem + 256, tDQ = tmem + 384;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmdo);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      const int qrow = int(int64_t(j) * sh.rows + tile.row0);
+      mbar_expect_tx(bar(B_QFULL), 4 * L::TILE);
+      for (int cb = 0; cb < 2; ++cb) {
+        tma_load_3d(sbase + L::q + cb * L::TILE, &tmq, bar(B_QFULL), cb * 64, h, qrow);
+        tma_load_3d(sbase + L::go + cb * L::TILE, &tmdo, bar(B_QFULL), cb * 64, h, qrow);
+      }
+      BlockIter it;
+      it.init(tb.fseg, tile.seg0, tile.nseg);
+      for (int i = 0; it.valid(); ++i, it.next()) {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        const int key = it.cur.k0 + it.kb;
+        if (!mbar_wait(bar(B_KEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
+        mbar_expect_tx(bar(B_KFULL + st), 2 * L::TILE);
+        for (int cb = 0; cb < 2; ++cb)
+          tma_load_3d(sbase + L::k + (st * 2 + cb) * L::TILE, &tmk, bar(B_KFULL + st), cb * 64, kvh, key);
+        if (!mbar_wait(bar(B_VEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
+        mbar_expect_tx(bar(B_VFULL + st), 2 * L::TILE);
+        for (int cb = 0; cb < 2; ++cb)
+          tma_load_3d(sbase + L::v + (st * 2 + cb) * L::TILE, &tmv, bar(B_VFULL + st), cb * 64, kvh, key);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, KBN, false, false);  // S, dP
+      constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);     // dQ (K as MN-major B)
+      auto issue_s_dp = [&](int i) -> bool {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait(bar(B_KFULL + st), ph, tb.status, abort_flag)) return false;
+        if (!mbar_wait(bar(B_SEMPTY + st), ph ^ 1, tb.status, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
+          tc_mma(tS + st * KBN, smem_desc_sw128(sbase + L::q + off, 16, 1024),
+                 smem_desc_sw128(sbase + L::k + st * 2 * L::TILE + off, 16, 1024), id_s, kk > 0);
+        }
+        tc_commit(bar(B_SFULL + st));
+        if (!mbar_wait(bar(B_VFULL + st), ph, tb.status, abort_flag)) return false;
+        if (!mbar_wait(bar(B_DPEMPTY), (i & 1) ^ 1, tb.status, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
+          tc_mma(tDP, smem_desc_sw128(sbase + L::go + off, 16, 1024),
+                 smem_desc_sw128(sbase + L::v + st * 2 * L::TILE + off, 16, 1024), id_s, kk > 0);
+        }
+        tc_commit(bar(B_DPFULL));
+        tc_commit(bar(B_VEMPTY + st));
+        return true;
+      };
+      auto issue_dq = [&](int i) -> bool {
+        const int st = i & 1;
+        if (!mbar_wait(bar(B_DSFULL), i & 1, tb.status, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t kbase = sbase + L::k + st * 2 * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < KBN / 16; ++kk)
+          tc_mma(tDQ, smem_desc_sw128(sbase + L::ds + (kk >> 2) * L::TILE + (kk & 3) * 32, 16, 1024),
+                 smem_desc_sw128(kbase + kk * 2048, L::TILE, 1024), id_q, (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(B_DSEMPTY));
+        tc_commit(bar(B_KEMPTY + st));
+        return true;
+      };
+      bool ok = mbar_wait(bar(B_QFULL), 0, tb.status, abort_flag);
+      BlockIter it;
+      it.init(tb.fseg, tile.seg0, tile.nseg);
+      int i = 0;
+      for (; ok && it.valid(); ++i, it.next()) {
+        if (!issue_s_dp(i)) { ok = false; break; }
+        if (i > 0 && !issue_dq(i - 1)) { ok = false; break; }
+      }
+      if (ok && i > 0) issue_dq(i - 1);
+    }
+  } else {
+    // ------------------------------------------------------------ compute (row = TMEM lane)
+    const int r = tid;
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const bool rok = r < tile.nrows;
+    float l2 = 0.f, delta = 0.f;
+    int lim = -1;
+    if (rok) {
+      const float4 rec = a.rowrec[(int64_t(j) * sh.Hq + h) * sh.rows + tile.row0 + r];
+      l2 = rec.x;
+      delta = rec.y;
+      lim = __float_as_int(rec.z);
+    }
+    BlockIter it;
+    it.init(tb.fseg, tile.seg0, tile.nseg);
+    int i = 0;
+    bool ok = true;
+    for (; it.valid(); ++i, it.next()) {
+      const int sb = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      const int nvalid = it.cur.nkeys - it.kb;
+      const int climit = !rok ? 0 : (it.cur.diag ? min(nvalid, lim - (it.cur.pos0 + it.kb) + 1) : nvalid);
+      if (!mbar_wait_warp(bar(B_SFULL + sb), ph, tb.status, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(B_DPFULL), i & 1, tb.status, abort_flag)) { ok = false; break; }
+      // the dS tile was last read by dQ(i - 1)
+      if (i >= 1 && !mbar_wait_warp(bar(B_DSEMPTY), (i - 1) & 1, tb.status, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t drow = sbase + L::ds + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+      for (int c32 = 0; c32 < KBN / 32; ++c32) {
+        float s[32], dp[32];
+        tmem_ld32(tS + lane_off + sb * KBN + c32 * 32, s);
+        tmem_ld32(tDP + lane_off + c32 * 32, dp);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int c = c32 * 32 + e;
+          const float p = c < climit ? ex2_approx(fmaf(s[e], sh.scale_log2, -l2)) : 0.f;
+          s[e] = p * (dp[e] - delta);
+        }
+        // 32 keys = four 16-byte chunks of this row's 128-byte line in block c32 / 2
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int c = (c32 & 1) * 4 + q4;  // chunk within the 64-key block
+          const uint32_t addr = drow + (c32 >> 1) * L::TILE + (((c ^ (r & 7))) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
+                       "r"(pack_bf16(s[8 * q4], s[8 * q4 + 1])), "r"(pack_bf16(s[8 * q4 + 2], s[8 * q4 + 3])),
+                       "r"(pack_bf16(s[8 * q4 + 4], s[8 * q4 + 5])), "r"(pack_bf16(s[8 * q4 + 6], s[8 * q4 + 7]))
+                       : "memory");
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_SEMPTY + sb));
+        mbar_arrive(bar(B_DPEMPTY));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DSFULL));
+    }
+    // epilogue: dQ (main part, scaled) -> fp32 accumulator row, written once
+    if (ok && i > 0 && mbar_wait_warp(bar(B_DSEMPTY), (i - 1) & 1, tb.status, abort_flag)) {
+      tc_fence_after();
+      const int64_t qrow = (int64_t(j) * sh.rows + tile.row0 + r) * sh.Hq + h;
+      float4* dst = reinterpret_cast<float4*>(a.dqacc + qrow * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(tDQ + lane_off + c * 32, o);
+        tmem_wait_ld();
+        if (rok) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[c * 8 + e] = make_float4(sh.scale * o[4 * e], sh.scale * o[4 * e + 1], sh.scale * o[4 * e + 2],
+                                         sh.scale * o[4 * e + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+
+cudaError_t encoder() {
+  std::call_once(g_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+cudaError_t map3d(CUtensorMap* m, const void* base, int heads, int64_t rows) {
+  const cuuint64_t dims[3] = {128, cuuint64_t(heads), cuuint64_t(rows)};
+  const cuuint64_t strides[2] = {256, cuuint64_t(heads) * 256};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t ba_launch_main_bwd_q_tc(const BaBwdArgs& a, cudaStream_t st) {
+  const int64_t grid = int64_t(a.tb.n_fq) * a.sh.steps * a.sh.Hq;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL || a.sh.d != 128) return cudaErrorInvalidConfiguration;
+  cudaError_t e = encoder();
+  if (e != cudaSuccess) return e;
+  const int64_t qrows = int64_t(a.sh.steps) * a.sh.rows;
+  CUtensorMap mq, mdo, mk, mv;
+  if ((e = map3d(&mq, a.qp, a.sh.Hq, qrows)) != cudaSuccess) return e;
+  if ((e = map3d(&mdo, a.dop, a.sh.Hq, qrows)) != cudaSuccess) return e;
+  if ((e = map3d(&mk, a.kmp, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  if ((e = map3d(&mv, a.vmp, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  const int smem = int(DqSmem::alloc);
+  if ((e = cudaFuncSetAttribute(main_bwd_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+      cudaSuccess)
+    return e;
+  main_bwd_q_tc_kernel<<<unsigned(grid), NTHREADS, smem, st>>>(a, mq, mdo, mk, mv);
+  return cudaGetLastError();
+}

@@ -1,5 +1,5 @@
-// K6 — causal main-sequence attention backward on the 5th-generation tensor
-// cores (tcgen05 / TMEM / TMA), key-stationary.
+// K6 (dK / dV part) — gradient of the main keys and values on the tcgen05
+// tensor cores, key-stationary.
 //
 // "Online Draft Co-Training ...", rainbus page, method step 5 and core method:
 // the backward replays the same ring and accumulates gradients locally, with
@@ -9,22 +9,20 @@
 // of its group.  P is recomputed from the merged lse (exact for both key sets,
 // because Eq. 2's merged result is the single softmax over their union).
 //
-// Per (query tile, key tile) pair, all on the tensor cores:
-//   S^T  = K Q^T        M=128 keys, N=64 queries, K=d        -> TMEM
-//   dP^T = V dO^T       same                                  -> TMEM
+// Per (query tile, key tile) pair, on the tensor cores:
+//   S^T  = K Q^T        M=128 keys, N=64 queries, K=d        -> TMEM (2 buffers)
+//   dP^T = V dO^T       same                                  -> TMEM (2 buffers)
 //   (threads)  P^T = exp2(S^T * scale*log2e - lse*log2e),  dS^T = P^T (dP^T - Delta)
 //              written as bf16 into 128B-swizzled shared tiles [key][query]
 //   dV  += P^T dO       M=128 keys, N=d, K=64 queries (dO as an MN-major operand)
 //   dK  += dS^T Q       same
-//   dQ^T = K^T dS^T     M=d, N=64 queries, K=128 keys (K and dS^T read MN-major)
-//   (threads)  dQ^T -> per-warp fp32 staging tiles [query][32 d] -> TMA bulk
-//              reduce-add into the fp32 dQ accumulator (scaled).
 // dK and dV stay in TMEM for the whole CTA and are written once, in natural
-// order, at the end.  TMEM: S^T / dQ^T buffers [0,64) and [64,128), dP^T
-// buffers [128,192) and [192,256), dK [256,384), dV [384,512).
-// Warp roles: warps 0-3 compute (TMEM lane = key row for S^T/dP^T/dK/dV, = d
-// row for dQ^T), warp 4 loads (TMA for tiles, plain loads for lse/Delta/limits),
-// warp 5 issues the MMAs and owns TMEM.  All waits are bounded.
+// order, at the end.  dQ is computed by the query-stationary kernel
+// (main_bwd_q_tc.cu), which needs no atomics.  TMEM: S^T buffers [0,64) and
+// [64,128), dP^T buffers [128,192) and [192,256), dK [256,384), dV [384,512).
+// Warp roles: warps 0-3 compute (TMEM lane = key row), warp 4 loads with TMA
+// (Q, dO and the tile's 16-byte row records {lse*log2e, Delta, key limit}) into
+// a 3-stage ring, warp 5 issues the MMAs and owns TMEM.  All waits are bounded.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -39,32 +37,33 @@ constexpr int KBN = 128;  // keys per CTA
 constexpr int QBM = 64;   // queries per tile
 constexpr int NTHREADS = 192;
 
+constexpr int NQS = 3;    // query-tile pipeline stages
+
 struct BwdSmem {
   static constexpr uint32_t KT = 128u * 128u;  // [128 keys][64 d] bf16 block
   static constexpr uint32_t QT = 64u * 128u;   // [64 queries][64 d] bf16 block
+  static constexpr uint32_t META = 64 * 16;    // 64 row records {lse*log2e, Delta, limit, 0}
   static constexpr uint32_t k = 0;             // 2 blocks
   static constexpr uint32_t v = k + 2 * KT;
-  static constexpr uint32_t q = v + 2 * KT;    // [2 stages][2 blocks]
-  static constexpr uint32_t go = q + 4 * QT;   // [2 stages][2 blocks]
-  static constexpr uint32_t pt = go + 4 * QT;  // P^T  [128 keys][64 queries] bf16
-  static constexpr uint32_t dst = pt + KT;     // dS^T [128 keys][64 queries] bf16
-  static constexpr uint32_t dqs = dst + KT;    // dQ staging fp32, per warp [64][32]
-  static constexpr uint32_t META = 3 * 64 * 4 + 16;
-  static constexpr uint32_t meta = dqs + 64 * 128 * 4;  // [2 stages] l2[64], dl[64], lim[64], nrows
-  static constexpr uint32_t bars = meta + 2 * META;
+  static constexpr uint32_t q = v + 2 * KT;    // [NQS stages][2 blocks]
+  static constexpr uint32_t go = q + NQS * 2 * QT;
+  static constexpr uint32_t meta = go + NQS * 2 * QT;  // [NQS stages]
+  // P^T then dS^T, [128 keys][64 queries] bf16 each
+  static constexpr uint32_t pt = meta + NQS * META;
+  static constexpr uint32_t dst = pt + KT;
+  static constexpr uint32_t bars = dst + KT;
   static constexpr uint32_t bytes = bars + 256;
   static constexpr uint32_t alloc = bytes + 1024;
 };
 
 enum {
   B_KV = 0,
-  B_QFULL = 1,   // [2]
-  B_QEMPTY = 3,  // [2]
-  B_SFULL = 5,   // [2]
-  B_SEMPTY = 7,  // [2]
-  B_PFULL = 9,
-  B_PEMPTY = 10,
-  B_DQFULL = 11, // [2]
+  B_QFULL = 1,   // [NQS]
+  B_QEMPTY = 4,  // [NQS]
+  B_SFULL = 7,   // [2]
+  B_SEMPTY = 9,  // [2]
+  B_PFULL = 11,
+  B_PEMPTY = 12,
   B_DONE = 13,
   B_COUNT = 14
 };
@@ -97,21 +96,11 @@ struct QIter {
   }
 };
 
-__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-    main_bwd_tc_kernel(const BaBwdArgs a, const __grid_constant__ CUtensorMap tmq,
-                       const __grid_constant__ CUtensorMap tmdo, const __grid_constant__ CUtensorMap tmk,
-                       const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdq) {
+    main_bwd_kv_tc_kernel(const BaBwdArgs a, const __grid_constant__ CUtensorMap tmq,
+                          const __grid_constant__ CUtensorMap tmdo, const __grid_constant__ CUtensorMap tmk,
+                          const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmrec) {
   using L = BwdSmem;
   constexpr int D = 128;
   extern __shared__ unsigned char smem_raw[];
@@ -139,12 +128,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(bar(B_KV), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_QFULL + s), 2);
+    for (int s = 0; s < NQS; ++s) {
+      mbar_init(bar(B_QFULL + s), 1);
       mbar_init(bar(B_QEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
       mbar_init(bar(B_SEMPTY + s), 4);
-      mbar_init(bar(B_DQFULL + s), 1);
     }
     mbar_init(bar(B_PFULL), 4);
     mbar_init(bar(B_PEMPTY), 1);
@@ -169,7 +159,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&tmdo);
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
-      tma_prefetch_desc(&tmdq);
+      tma_prefetch_desc(&tmrec);
       if (any) {
         mbar_expect_tx(bar(B_KV), 4 * L::KT);
         for (int cb = 0; cb < 2; ++cb) {
@@ -178,59 +168,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-    QIter it;
-    it.init(tb.bqr, kt.qr0, kt.nqr, nstream);
-    for (int i = 0; it.valid(); ++i, it.next()) {
-      const int st = i & 1;
-      const uint32_t ph = (i >> 1) & 1;
-      if (!mbar_wait_warp(bar(B_QEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
-      const BaQTile qt = tb.bq[it.ti];
-      const int j = it.sx / sh.G, h = kvh * sh.G + it.sx % sh.G;
-      const int qrow = int(int64_t(j) * sh.rows + qt.row0);
-      if (lane == 0) {
-        mbar_expect_tx(bar(B_QFULL + st), 4 * L::QT);
+    if (lane == 0) {
+      QIter it;
+      it.init(tb.bqr, kt.qr0, kt.nqr, nstream);
+      for (int i = 0; it.valid(); ++i, it.next()) {
+        const int st = i % NQS;
+        const uint32_t ph = (i / NQS) & 1;
+        if (!mbar_wait(bar(B_QEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
+        const BaQTile qt = tb.bq[it.ti];
+        const int j = it.sx / sh.G, h = kvh * sh.G + it.sx % sh.G;
+        const int qrow = int(int64_t(j) * sh.rows + qt.row0);
+        const int srow = int((int64_t(j) * sh.Hq + h) * sh.rows + qt.row0);
+        mbar_expect_tx(bar(B_QFULL + st), 4 * L::QT + L::META);
         for (int cb = 0; cb < 2; ++cb) {
           tma_load_3d(sbase + L::q + (st * 2 + cb) * L::QT, &tmq, bar(B_QFULL + st), cb * 64, h, qrow);
           tma_load_3d(sbase + L::go + (st * 2 + cb) * L::QT, &tmdo, bar(B_QFULL + st), cb * 64, h, qrow);
         }
+        tma_load_2d(sbase + L::meta + st * L::META, &tmrec, bar(B_QFULL + st), 0, srow);
       }
-      float* l2 = reinterpret_cast<float*>(gbase + L::meta + st * L::META);
-      float* dl = l2 + 64;
-      int* lim = reinterpret_cast<int*>(dl + 64);
-      const int64_t srow0 = (int64_t(j) * sh.Hq + h) * sh.rows + qt.row0;
-      for (int r = lane; r < QBM; r += 32) {
-        const bool ok = r < qt.nrows;
-        l2[r] = ok ? a.lsep[srow0 + r] * BA_LOG2E : INFINITY;
-        dl[r] = ok ? a.dlt[srow0 + r] : 0.f;
-        lim[r] = ok ? tb.row_lim[qt.row0 + r] : -1;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_QFULL + st));
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one() && any) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, QBM, false, false);   // S^T, dP^T
       constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);     // dV, dK
-      constexpr uint32_t id_q = idesc_bf16_f32(128, QBM, true, true);     // dQ^T
       int n = 0;
       for (int r = kt.qr0; r < kt.qr0 + kt.nqr; ++r) n += (tb.bqr[r].t1 - tb.bqr[r].t0) * nstream;
       auto issue_sdp = [&](int i) -> bool {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait(bar(B_QFULL + st), ph, tb.status, abort_flag)) return false;
-        if (!mbar_wait(bar(B_SEMPTY + st), ph ^ 1, tb.status, abort_flag)) return false;
+        const int qs = i % NQS;
+        const int sb = i & 1;
+        if (!mbar_wait(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) return false;
+        if (!mbar_wait(bar(B_SEMPTY + sb), ((i >> 1) & 1) ^ 1, tb.status, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ok_ = (kk >> 2) * L::KT + (kk & 3) * 32;
           const uint32_t oq = (kk >> 2) * L::QT + (kk & 3) * 32;
-          tc_mma(tS + st * 64, smem_desc_sw128(sbase + L::k + ok_, 16, 1024),
-                 smem_desc_sw128(sbase + L::q + st * 2 * L::QT + oq, 16, 1024), id_s, kk > 0);
-          tc_mma(tDP + st * 64, smem_desc_sw128(sbase + L::v + ok_, 16, 1024),
-                 smem_desc_sw128(sbase + L::go + st * 2 * L::QT + oq, 16, 1024), id_s, kk > 0);
+          tc_mma(tS + sb * 64, smem_desc_sw128(sbase + L::k + ok_, 16, 1024),
+                 smem_desc_sw128(sbase + L::q + qs * 2 * L::QT + oq, 16, 1024), id_s, kk > 0);
+          tc_mma(tDP + sb * 64, smem_desc_sw128(sbase + L::v + ok_, 16, 1024),
+                 smem_desc_sw128(sbase + L::go + qs * 2 * L::QT + oq, 16, 1024), id_s, kk > 0);
         }
-        tc_commit(bar(B_SFULL + st));
+        tc_commit(bar(B_SFULL + sb));
         return true;
       };
       bool ok = mbar_wait(bar(B_KV), 0, tb.status, abort_flag);
@@ -239,8 +218,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (i + 1 < n && !issue_sdp(i + 1)) break;
         if (!mbar_wait(bar(B_PFULL), i & 1, tb.status, abort_flag)) break;
         tc_fence_after();
-        const int st = i & 1;
-        const uint32_t qb = sbase + L::q + st * 2 * L::QT, gb = sbase + L::go + st * 2 * L::QT;
+        const int qs = i % NQS;
+        const uint32_t qb = sbase + L::q + qs * 2 * L::QT, gb = sbase + L::go + qs * 2 * L::QT;
 #pragma unroll
         for (int kk = 0; kk < QBM / 16; ++kk) {
           tc_mma(tDV, smem_desc_sw128(sbase + L::pt + kk * 32, 16, 1024),
@@ -248,13 +227,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tc_mma(tDK, smem_desc_sw128(sbase + L::dst + kk * 32, 16, 1024),
                  smem_desc_sw128(qb + kk * 2048, L::QT, 1024), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
         }
-#pragma unroll
-        for (int kk = 0; kk < KBN / 16; ++kk)
-          tc_mma(tS + st * 64, smem_desc_sw128(sbase + L::k + kk * 2048, L::KT, 1024),
-                 smem_desc_sw128(sbase + L::dst + kk * 2048, L::KT, 1024), id_q, kk > 0);
-        tc_commit(bar(B_DQFULL + st));
-        tc_commit(bar(B_QEMPTY + st));
         tc_commit(bar(B_PEMPTY));
+        tc_commit(bar(B_QEMPTY + qs));
       }
       tc_commit(bar(B_DONE));
     }
@@ -268,32 +242,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bool ok = true;
     int i = 0;
     for (; it.valid(); ++i, it.next()) {
-      const int st = i & 1;
+      const int qs = i % NQS, sb = i & 1;
       const uint32_t ph = (i >> 1) & 1;
       const BaQTile qt = tb.bq[it.ti];
       const int j = it.sx / sh.G, h = kvh * sh.G + it.sx % sh.G;
       const bool diag = it.cur.diag != 0;
-      // q_full: acquire the loader's plain stores of lse / Delta / limits
-      if (!mbar_wait_warp(bar(B_QFULL + st), ph, tb.status, abort_flag)) { ok = false; break; }
-      if (!mbar_wait_warp(bar(B_SFULL + st), ph, tb.status, abort_flag)) { ok = false; break; }
+      // q_full: the row records of this tile are in shared memory
+      if (!mbar_wait_warp(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(B_SFULL + sb), ph, tb.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
       float s[QBM], dp[QBM];
-      tmem_ld32(tS + lane_off + st * 64, s);
-      tmem_ld32(tS + lane_off + st * 64 + 32, s + 32);
-      tmem_ld32(tDP + lane_off + st * 64, dp);
-      tmem_ld32(tDP + lane_off + st * 64 + 32, dp + 32);
+      tmem_ld32(tS + lane_off + sb * 64, s);
+      tmem_ld32(tS + lane_off + sb * 64 + 32, s + 32);
+      tmem_ld32(tDP + lane_off + sb * 64, dp);
+      tmem_ld32(tDP + lane_off + sb * 64 + 32, dp + 32);
       tmem_wait_ld();
-      const float* l2 = reinterpret_cast<const float*>(gbase + L::meta + st * L::META);
-      const float* dl = l2 + 64;
-      const int* lim = reinterpret_cast<const int*>(dl + 64);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SEMPTY + sb));  // S^T / dP^T buffers are free again
+      // row records {lse*log2e, Delta, limit, 0}; rows past the tile are masked
+      const float* rec = reinterpret_cast<const float*>(gbase + L::meta + qs * L::META);
+      const int nrows = qt.nrows;
 #pragma unroll
       for (int c = 0; c < QBM; ++c) {
-        const bool v = kok && c < qt.nrows && (!diag || kpos <= lim[c]);
-        const float p = v ? ex2_approx(fmaf(s[c], sh.scale_log2, -l2[c])) : 0.f;
+        const bool v = kok && c < nrows && (!diag || kpos <= __float_as_int(rec[4 * c + 2]));
+        const float p = v ? ex2_approx(fmaf(s[c], sh.scale_log2, -rec[4 * c])) : 0.f;
         s[c] = p;
-        dp[c] = p * (dp[c] - dl[c]);
+        dp[c] = p * (dp[c] - rec[4 * c + 1]);
       }
-      // P^T and dS^T are free once the MMAs of the previous pair have read them
+      // P^T / dS^T are free once dV / dK of the previous pair have read them
       if (i >= 1 && !mbar_wait_warp(bar(B_PEMPTY), (i - 1) & 1, tb.status, abort_flag)) { ok = false; break; }
       const uint32_t rowoff = (tid >> 3) * 1024 + (tid & 7) * 128;
 #pragma unroll
@@ -312,31 +289,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL));
-      // dQ^T of this pair: TMEM lane = d, columns = queries
-      if (!mbar_wait_warp(bar(B_DQFULL + st), ph, tb.status, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      tmem_ld32(tS + lane_off + st * 64, s);
-      tmem_ld32(tS + lane_off + st * 64 + 32, s + 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SEMPTY + st));
-      // each warp stages its 32 d-columns as [query][32] fp32 and adds them into
-      // the accumulator with its own bulk reduce (no cross-warp barrier)
-      if (lane == 0) bulk_wait_read0();
-      __syncwarp();
-      float* stage = reinterpret_cast<float*>(gbase + L::dqs + warp * (QBM * 32 * 4));
-#pragma unroll
-      for (int c = 0; c < QBM; ++c) stage[c * 32 + lane] = s[c] * sh.scale;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_reduce_add_3d(&tmdq, sbase + L::dqs + warp * (QBM * 32 * 4), warp * 32, h,
-                          int(int64_t(j) * sh.rows + qt.row0));
-        bulk_commit();
-      }
     }
-    if (lane == 0) bulk_wait0();
     // epilogue: dK (scaled) and dV of this key tile, natural order
     auto* dkm = static_cast<__nv_bfloat16*>(a.dkm);
     auto* dvm = static_cast<__nv_bfloat16*>(a.dvm);
@@ -408,14 +361,14 @@ cudaError_t map3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int 
 
 bool ba_main_bwd_tc_supported(const BaShape& sh) { return sh.d == 128; }
 
-cudaError_t ba_launch_main_bwd_tc(const BaBwdArgs& a, cudaStream_t st) {
+cudaError_t ba_launch_main_bwd_kv_tc(const BaBwdArgs& a, cudaStream_t st) {
   const int64_t grid = int64_t(a.tb.n_bkv) * a.sh.Hkv;
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL || a.sh.d != 128) return cudaErrorInvalidConfiguration;
   cudaError_t e = encoder();
   if (e != cudaSuccess) return e;
   const int64_t qrows = int64_t(a.sh.steps) * a.sh.rows;
-  CUtensorMap mq, mdo, mk, mv, mdq;
+  CUtensorMap mq, mdo, mk, mv;
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if ((e = map3d(&mq, a.qp, bf, 2, 128, a.sh.Hq, qrows, 64, QBM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
   if ((e = map3d(&mdo, a.dop, bf, 2, 128, a.sh.Hq, qrows, 64, QBM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
@@ -424,13 +377,21 @@ cudaError_t ba_launch_main_bwd_tc(const BaBwdArgs& a, cudaStream_t st) {
     return e;
   if ((e = map3d(&mv, a.vmp, bf, 2, 128, a.sh.Hkv, a.sh.T, 64, KBN, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
-  if ((e = map3d(&mdq, a.dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, a.sh.Hq, qrows, 32, QBM,
-                 CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
-    return e;
+  CUtensorMap mrec;
+  {
+    const cuuint64_t dims[2] = {4, cuuint64_t(qrows) * a.sh.Hq};
+    const cuuint64_t strides[1] = {16};
+    const cuuint32_t box[2] = {4, QBM};
+    const cuuint32_t es[2] = {1, 1};
+    if (g_encode(&mrec, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.rowrec, dims, strides, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   const int smem = int(BwdSmem::alloc);
-  if ((e = cudaFuncSetAttribute(main_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+  if ((e = cudaFuncSetAttribute(main_bwd_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
       cudaSuccess)
     return e;
-  main_bwd_tc_kernel<<<unsigned(grid), NTHREADS, smem, st>>>(a, mq, mdo, mk, mv, mdq);
+  main_bwd_kv_tc_kernel<<<unsigned(grid), NTHREADS, smem, st>>>(a, mq, mdo, mk, mv, mrec);
   return cudaGetLastError();
 }

@@ -245,19 +245,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int c = 0; c < TBN; ++c)
           if (c >= climit) s[c] = -INFINITY;
       }
-      float mx = -INFINITY;
+      // row max as 8 independent chains (a single chain is 128 dependent steps)
+      float mxp[8];
 #pragma unroll
-      for (int c = 0; c < TBN; ++c) mx = fmaxf(mx, s[c]);
+      for (int k = 0; k < 8; ++k) mxp[k] = s[k];
+#pragma unroll
+      for (int c = 8; c < TBN; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mxp[k] = fmaxf(mxp[k], mxp[k + 4]);
+      const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
       const float m_blk = mx * sh.scale_log2;
       const bool grow = m_blk > m_used + 8.f;
       const float m_next = grow ? m_blk : m_used;
       const float base = m_next == -INFINITY ? 0.f : m_next;
-      float rs = 0.f;
+      float rsp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < TBN; ++c) {
         s[c] = ex2_approx(fmaf(s[c], sh.scale_log2, -base));
-        rs += s[c];
+        rsp[c & 7] += s[c];
       }
+      const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
       // the P buffer was last read by PV(i - 2)
       if (i >= 2 && !mbar_wait_warp(bar(B_ODONE + sb), ((i - 2) >> 1) & 1, tb.status, abort_flag)) {
         ok = false;

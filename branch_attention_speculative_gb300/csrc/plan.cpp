@@ -327,8 +327,7 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
   w.lb = f; f = align256(f + (fam == BA_FAMILY_CAUSAL ? 0 : qrows * 4));
   size_t b = scratch;
   w.dop = b; b = align256(b + qrows * dd * 2);
-  w.dlt = b; b = align256(b + qrows * 4);
-  w.lsep = b; b = align256(b + qrows * 4);
+  w.rowrec = b; b = align256(b + qrows * 16);
   w.dqacc = b; b = align256(b + qrows * dd * 4);
   w.total = std::max(f, b);
 

@@ -17,7 +17,7 @@ struct BaWorkspaceLayout {
   size_t t_row_lim, t_tok_perm, t_anc_perm, t_fq, t_fseg, t_forder, t_bq, t_bkv, t_bqr, t_border;
   size_t qp, kmp, vmp, kbp, vbp;  // zigzag-packed inputs (bf16)
   size_t om, lm, ob, lb;          // forward partials (fp32)
-  size_t dop, dlt, lsep, dqacc;   // backward scratch: packed dO (bf16), Delta, lse, dQ (fp32)
+  size_t dop, rowrec, dqacc;      // backward scratch: packed dO (bf16), row records (16 B), dQ (fp32)
   size_t total;
 };
 
@@ -61,8 +61,8 @@ struct ba_plan {
   std::vector<void*> prof_events;                  // pool, pairs (start, stop)
   size_t prof_used = 0;                            // pairs recorded since the last read
   std::vector<int> prof_kernel;                    // kernel id of each recorded pair
-  double prof_ms[8] = {0};
-  int64_t prof_launches[8] = {0};
+  double prof_ms[16] = {0};
+  int64_t prof_launches[16] = {0};
 
   ~ba_plan();
 };

@@ -2,9 +2,10 @@
 //
 // For every query-head row: Delta = <dO, O> in fp32 (the row term of the
 // softmax backward, dS = P * (dP - Delta)); dO and lse are gathered into the
-// packed zigzag order the main backward reads (Delta and lse stream-major,
-// [step][head][row], so a query tile's values are contiguous); the row of the
-// fp32 dQ accumulator is zeroed.  The pages only say that the backward replays the
+// packed zigzag order the main backward reads; lse (in base 2), Delta and the
+// row's key limit go into one 16-byte record per (step, head, row), stored
+// stream-major so that a query tile's records are one contiguous TMA box; the
+// row of the fp32 dQ accumulator is zeroed.  The pages only say that the backward replays the
 // ring ("Online Draft Co-Training ...", rainbus page, method step 5); Delta is
 // what that replay needs per row when P is recomputed from the merged lse.
 // HBM-bound: d/8 threads per row, 16-byte loads.
@@ -52,10 +53,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BaBwdArgs a) {
     float4* dq = reinterpret_cast<float4*>(a.dqacc + row * D);
     dq[2 * sub] = make_float4(0.f, 0.f, 0.f, 0.f);
     dq[2 * sub + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (sub == 0) {  // Delta and lse stream-major: [step][head][row]
+    if (sub == 0) {  // one 16-byte record per (step, head, row), stream-major
       const int64_t srow = (j * sh.Hq + h) * sh.rows + r;
-      a.dlt[srow] = acc;
-      a.lsep[srow] = a.lse[nrow];
+      a.rowrec[srow] = make_float4(a.lse[nrow] * BA_LOG2E, acc, __int_as_float(a.tb.row_lim[r]), 0.f);
     }
   }
 }
