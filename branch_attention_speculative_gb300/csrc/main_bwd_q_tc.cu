@@ -17,7 +17,9 @@
 // fp32 dQ accumulator (no atomics, no read-modify-write); the branch backward
 // adds the branch part and writes the bf16 result.
 // TMEM: S0 [0,128), S1 [128,256), dP [256,384), dQ [384,512).
-// Warps: 0-3 compute (thread = query row = TMEM lane), 4 TMA, 5 MMA + TMEM.
+// Warps: 0-7 compute (warp w: TMEM lane quarter w % 4 = query rows, keys
+// 64 (w / 4) .. of each block; two warps per SM sub-partition hide each other's
+// latencies), 8 TMA, 9 MMA + TMEM.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -30,7 +32,7 @@ namespace {
 
 constexpr int QBM = 128;  // query rows per tile (BA_FWD_BM)
 constexpr int KBN = 128;  // keys per block
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;  // 8 compute warps, 1 TMA warp, 1 MMA warp
 
 struct DqSmem {
   static constexpr uint32_t TILE = 128u * 128u;  // [128 rows][64 columns] bf16, swizzled
@@ -122,15 +124,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SEMPTY + s), 4);
+      mbar_init(bar(B_SEMPTY + s), 8);
     }
     mbar_init(bar(B_DPFULL), 1);
-    mbar_init(bar(B_DPEMPTY), 4);
-    mbar_init(bar(B_DSFULL), 4);
+    mbar_init(bar(B_DPEMPTY), 8);
+    mbar_init(bar(B_DSFULL), 8);
     mbar_init(bar(B_DSEMPTY), 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
     tmem_relinquish();
   }
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tDP = tmem + 256, tDQ = tmem + 384;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
       tma_prefetch_desc(&tmq);
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tma_load_3d(sbase + L::v + (st * 2 + cb) * L::TILE, &tmv, bar(B_VFULL + st), cb * 64, kvh, key);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, KBN, false, false);  // S, dP
@@ -224,9 +226,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (ok && i > 0) issue_dq(i - 1);
     }
   } else {
-    // ------------------------------------------------------------ compute (row = TMEM lane)
-    const int r = tid;
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    // ------------------------------------------------------------ compute
+    // warp w: TMEM lane quarter w % 4 (query rows 32 (w % 4) ..), keys
+    // 64 (w / 4) .. 64 (w / 4) + 63 of each 128-key block
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const bool rok = r < tile.nrows;
     float l2 = 0.f, delta = 0.f;
     int lim = -1;
@@ -252,7 +257,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       const uint32_t drow = sbase + L::ds + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-      for (int c32 = 0; c32 < KBN / 32; ++c32) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c32 = half * 2 + cc;
         float s[32], dp[32];
         tmem_ld32(tS + lane_off + sb * KBN + c32 * 32, s);
         tmem_ld32(tDP + lane_off + c32 * 32, dp);
@@ -284,15 +290,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DSFULL));
     }
-    // epilogue: dQ (main part, scaled) -> fp32 accumulator row, written once
+    // epilogue: dQ (main part, scaled) -> fp32 accumulator row, written once;
+    // each warp writes d-columns 64 (w / 4) .. of its 32 rows
     if (ok && i > 0 && mbar_wait_warp(bar(B_DSEMPTY), (i - 1) & 1, tb.status, abort_flag)) {
       tc_fence_after();
       const int64_t qrow = (int64_t(j) * sh.rows + tile.row0 + r) * sh.Hq + h;
-      float4* dst = reinterpret_cast<float4*>(a.dqacc + qrow * D);
+      float4* dst = reinterpret_cast<float4*>(a.dqacc + qrow * D + half * 64);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float o[32];
-        tmem_ld32(tDQ + lane_off + c * 32, o);
+        tmem_ld32(tDQ + lane_off + half * 64 + c * 32, o);
         tmem_wait_ld();
         if (rok) {
 #pragma unroll
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -20,9 +20,11 @@
 // order, at the end.  dQ is computed by the query-stationary kernel
 // (main_bwd_q_tc.cu), which needs no atomics.  TMEM: S^T buffers [0,64) and
 // [64,128), dP^T buffers [128,192) and [192,256), dK [256,384), dV [384,512).
-// Warp roles: warps 0-3 compute (TMEM lane = key row), warp 4 loads with TMA
-// (Q, dO and the tile's 16-byte row records {lse*log2e, Delta, key limit}) into
-// a 3-stage ring, warp 5 issues the MMAs and owns TMEM.  All waits are bounded.
+// Warp roles: warps 0-7 compute (warp w: TMEM lane quarter w % 4 = key rows,
+// query columns 32 (w / 4) ..; two warps per SM sub-partition hide each
+// other's latencies), warp 8 loads with TMA (Q, dO and the tile's 16-byte row
+// records {lse*log2e, Delta, key limit}) into a 3-stage ring, warp 9 issues the
+// MMAs and owns TMEM.  All waits are bounded.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -35,7 +37,7 @@ namespace {
 
 constexpr int KBN = 128;  // keys per CTA
 constexpr int QBM = 64;   // queries per tile
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;  // 8 compute warps, 1 TMA warp, 1 MMA warp
 
 constexpr int NQS = 3;    // query-tile pipeline stages
 
@@ -134,14 +136,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SEMPTY + s), 4);
+      mbar_init(bar(B_SEMPTY + s), 8);
     }
-    mbar_init(bar(B_PFULL), 4);
+    mbar_init(bar(B_PFULL), 8);
     mbar_init(bar(B_PEMPTY), 1);
     mbar_init(bar(B_DONE), 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
     tmem_relinquish();
   }
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tS = tmem, tDP = tmem + 128, tDK = tmem + 256, tDV = tmem + 384;
   const bool any = kt.nqr > 0;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ loads
     if (lane == 0) {
       tma_prefetch_desc(&tmq);
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_load_2d(sbase + L::meta + st * L::META, &tmrec, bar(B_QFULL + st), 0, srow);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one() && any) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, QBM, false, false);   // S^T, dP^T
@@ -233,10 +235,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_commit(bar(B_DONE));
     }
   } else {
-    // ------------------------------------------------------------ compute (TMEM lane = tid)
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
-    const bool kok = tid < kt.nkeys;
-    const int kpos = kt.pos0 + tid;
+    // ------------------------------------------------------------ compute
+    // warp w: TMEM lane quarter w % 4 (key rows 32 (w % 4) ..), query columns
+    // 32 (w / 4) .. 32 (w / 4) + 31 of each 64-query tile
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const int col0 = half * 32;
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const bool kok = row < kt.nkeys;
+    const int kpos = kt.pos0 + row;
     QIter it;
     it.init(tb.bqr, kt.qr0, kt.nqr, nstream);
     bool ok = true;
@@ -245,44 +252,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int qs = i % NQS, sb = i & 1;
       const uint32_t ph = (i >> 1) & 1;
       const BaQTile qt = tb.bq[it.ti];
-      const int j = it.sx / sh.G, h = kvh * sh.G + it.sx % sh.G;
       const bool diag = it.cur.diag != 0;
       // q_full: the row records of this tile are in shared memory
       if (!mbar_wait_warp(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) { ok = false; break; }
       if (!mbar_wait_warp(bar(B_SFULL + sb), ph, tb.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      float s[QBM], dp[QBM];
-      tmem_ld32(tS + lane_off + sb * 64, s);
-      tmem_ld32(tS + lane_off + sb * 64 + 32, s + 32);
-      tmem_ld32(tDP + lane_off + sb * 64, dp);
-      tmem_ld32(tDP + lane_off + sb * 64 + 32, dp + 32);
+      float s[32], dp[32];
+      tmem_ld32(tS + lane_off + sb * 64 + col0, s);
+      tmem_ld32(tDP + lane_off + sb * 64 + col0, dp);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_SEMPTY + sb));  // S^T / dP^T buffers are free again
-      // row records {lse*log2e, Delta, limit, 0}; rows past the tile are masked
-      const float* rec = reinterpret_cast<const float*>(gbase + L::meta + qs * L::META);
-      const int nrows = qt.nrows;
+      // row records {lse*log2e, Delta, limit, 0}; queries past the tile are masked
+      const float* rec = reinterpret_cast<const float*>(gbase + L::meta + qs * L::META) + 4 * col0;
+      const int nq = qt.nrows - col0;
 #pragma unroll
-      for (int c = 0; c < QBM; ++c) {
-        const bool v = kok && c < nrows && (!diag || kpos <= __float_as_int(rec[4 * c + 2]));
-        const float p = v ? ex2_approx(fmaf(s[c], sh.scale_log2, -rec[4 * c])) : 0.f;
-        s[c] = p;
-        dp[c] = p * (dp[c] - rec[4 * c + 1]);
+      for (int c = 0; c < 32; ++c) {
+        const bool v = kok && c < nq && (!diag || kpos <= __float_as_int(rec[4 * c + 2]));
+        const float p = ex2_approx(fmaf(s[c], sh.scale_log2, -rec[4 * c]));
+        s[c] = v ? p : 0.f;
+        dp[c] = s[c] * (dp[c] - rec[4 * c + 1]);
       }
       // P^T / dS^T are free once dV / dK of the previous pair have read them
       if (i >= 1 && !mbar_wait_warp(bar(B_PEMPTY), (i - 1) & 1, tb.status, abort_flag)) { ok = false; break; }
-      const uint32_t rowoff = (tid >> 3) * 1024 + (tid & 7) * 128;
+      const uint32_t rowoff = (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-      for (int c = 0; c < QBM / 8; ++c) {
-        const uint32_t sw = ((c ^ (tid & 7)) << 4);
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint32_t sw = (((half * 4 + q4) ^ (row & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(sbase + L::pt + rowoff + sw),
-                     "r"(pack_bf16(s[8 * c], s[8 * c + 1])), "r"(pack_bf16(s[8 * c + 2], s[8 * c + 3])),
-                     "r"(pack_bf16(s[8 * c + 4], s[8 * c + 5])), "r"(pack_bf16(s[8 * c + 6], s[8 * c + 7]))
+                     "r"(pack_bf16(s[8 * q4], s[8 * q4 + 1])), "r"(pack_bf16(s[8 * q4 + 2], s[8 * q4 + 3])),
+                     "r"(pack_bf16(s[8 * q4 + 4], s[8 * q4 + 5])), "r"(pack_bf16(s[8 * q4 + 6], s[8 * q4 + 7]))
                      : "memory");
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(sbase + L::dst + rowoff + sw),
-                     "r"(pack_bf16(dp[8 * c], dp[8 * c + 1])), "r"(pack_bf16(dp[8 * c + 2], dp[8 * c + 3])),
-                     "r"(pack_bf16(dp[8 * c + 4], dp[8 * c + 5])), "r"(pack_bf16(dp[8 * c + 6], dp[8 * c + 7]))
+                     "r"(pack_bf16(dp[8 * q4], dp[8 * q4 + 1])), "r"(pack_bf16(dp[8 * q4 + 2], dp[8 * q4 + 3])),
+                     "r"(pack_bf16(dp[8 * q4 + 4], dp[8 * q4 + 5])), "r"(pack_bf16(dp[8 * q4 + 6], dp[8 * q4 + 7]))
                      : "memory");
       }
       fence_proxy_async_smem();
@@ -290,18 +294,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL));
     }
-    // epilogue: dK (scaled) and dV of this key tile, natural order
+    // epilogue: dK (scaled) and dV of this key tile, natural order; each warp
+    // writes d-columns 64 (w / 4) .. 64 (w / 4) + 63 of its 32 key rows
     auto* dkm = static_cast<__nv_bfloat16*>(a.dkm);
     auto* dvm = static_cast<__nv_bfloat16*>(a.dvm);
     const bool have = any && ok && i > 0 && mbar_wait_warp(bar(B_DONE), 0, tb.status, abort_flag);
     if (have) tc_fence_after();
-    const int64_t base = kok ? (int64_t(tb.tok_perm[kt.k0 + tid]) * sh.Hkv + kvh) * D : 0;
+    const int64_t base = kok ? (int64_t(tb.tok_perm[kt.k0 + row]) * sh.Hkv + kvh) * D + half * 64 : 0;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < 2; ++c) {
       float xk[32], xv[32];
       if (have) {
-        tmem_ld32(tDK + lane_off + c * 32, xk);
-        tmem_ld32(tDV + lane_off + c * 32, xv);
+        tmem_ld32(tDK + lane_off + half * 64 + c * 32, xk);
+        tmem_ld32(tDV + lane_off + half * 64 + c * 32, xv);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
