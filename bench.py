@@ -330,7 +330,9 @@ def run_ours(args, rank, world, local):
         e = kernels[dom]
         if e.get("unit") == "TFLOP/s":
             roofline = {"kernel": dom, "bound": "tensor", "achieved": e["achieved"], "peak": peak_t,
-                        "unit": "TFLOP/s", "frac": e["achieved"] / peak_t, "traffic": None,
+                        "unit": "TFLOP/s", "frac": e["achieved"] / peak_t,
+                        "traffic": measured_traffic(dom, wl.name),
+                        "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                         "peak_source": f"bf16_tflops_sustained ({peaks['source']})"}
         else:
             roofline = {"kernel": dom, "bound": "hbm", "achieved": e["achieved"], "peak": peaks["hbm_gbs"],
@@ -392,6 +394,39 @@ def resize_workload(wl, tokens: int):
         anchors = W.sample_anchors(np.random.default_rng(wl.seed), cu, per)
     return W.Workload(f"{wl.name}_T{tokens}", wl.family, cu, wl.heads_q, wl.heads_kv, wl.head_dim, wl.cp,
                       wl.depth, wl.block, anchors, wl.seed)
+
+
+KERNEL_SOURCES = {
+    "main_fwd": "main_fwd_tc.cu", "main_bwd_kv": "main_bwd_tc.cu", "main_bwd_dq": "main_bwd_q_tc.cu",
+}
+
+
+def source_sha256(kernel: str):
+    import hashlib
+    f = KERNEL_SOURCES.get(kernel)
+    if f is None:
+        return None
+    path = os.path.join(ROOT, "branch_attention_speculative_gb300", "csrc", f)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) of ``kernel`` on ``workload`` from
+    the committed ncu summary profiles/dram_traffic.md, or None when there is
+    no capture or the kernel's source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    want = source_sha256(kernel)
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 6 and cells[0] == kernel and cells[1] == workload:
+            try:
+                sha, rd, wr = cells[2], float(cells[3]), float(cells[4])
+            except ValueError:
+                continue
+            return rd + wr if sha == want else None
+    return None
 
 
 def _mem_available_bytes():

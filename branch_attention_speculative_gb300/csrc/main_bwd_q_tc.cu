@@ -256,35 +256,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (i >= 1 && !mbar_wait_warp(bar(B_DSEMPTY), (i - 1) & 1, tb.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t drow = sbase + L::ds + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c32 = half * 2 + cc;
-        float s[32], dp[32];
-        tmem_ld32(tS + lane_off + sb * KBN + c32 * 32, s);
-        tmem_ld32(tDP + lane_off + c32 * 32, dp);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = c32 * 32 + e;
-          const float p = c < climit ? ex2_approx(fmaf(s[e], sh.scale_log2, -l2)) : 0.f;
-          s[e] = p * (dp[e] - delta);
-        }
-        // 32 keys = four 16-byte chunks of this row's 128-byte line in block c32 / 2
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int c = (c32 & 1) * 4 + q4;  // chunk within the 64-key block
-          const uint32_t addr = drow + (c32 >> 1) * L::TILE + (((c ^ (r & 7))) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
-                       "r"(pack_bf16(s[8 * q4], s[8 * q4 + 1])), "r"(pack_bf16(s[8 * q4 + 2], s[8 * q4 + 3])),
-                       "r"(pack_bf16(s[8 * q4 + 4], s[8 * q4 + 5])), "r"(pack_bf16(s[8 * q4 + 6], s[8 * q4 + 7]))
-                       : "memory");
-        }
-      }
+      // this warp's 64 keys: both S and dP chunks loaded before one wait
+      float s[64], dp[64];
+      tmem_ld32(tS + lane_off + sb * KBN + half * 64, s);
+      tmem_ld32(tS + lane_off + sb * KBN + half * 64 + 32, s + 32);
+      tmem_ld32(tDP + lane_off + half * 64, dp);
+      tmem_ld32(tDP + lane_off + half * 64 + 32, dp + 32);
+      tmem_wait_ld();
+      // S and dP are in registers: their TMEM buffers can be refilled now
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(bar(B_SEMPTY + sb));
         mbar_arrive(bar(B_DPEMPTY));
+      }
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        const int c = half * 64 + e;
+        const float p = ex2_approx(fmaf(s[e], sh.scale_log2, -l2));
+        s[e] = (c < climit ? p : 0.f) * (dp[e] - delta);
+      }
+      // 64 keys = the eight 16-byte chunks of this row's line in block `half`
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t addr = drow + half * L::TILE + (((c ^ (r & 7))) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
+                     "r"(pack_bf16(s[8 * c], s[8 * c + 1])), "r"(pack_bf16(s[8 * c + 2], s[8 * c + 3])),
+                     "r"(pack_bf16(s[8 * c + 4], s[8 * c + 5])), "r"(pack_bf16(s[8 * c + 6], s[8 * c + 7]))
+                     : "memory");
       }
       fence_proxy_async_smem();
       __syncwarp();

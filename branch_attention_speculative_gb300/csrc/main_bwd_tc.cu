@@ -70,34 +70,45 @@ enum {
   B_COUNT = 14
 };
 
-// (query range, query tile, stream) iteration of one key tile
+// (stream, query range, query tile) iteration of one key tile.  The stream is
+// the outer loop: CTAs of neighbouring key tiles that run at the same time then
+// sweep the same stream's query tiles within a tile or two of each other, so
+// the Q / dO tiles they stream are shared in L2 (with the stream innermost the
+// shared window is ~28 tiles wide per CTA offset and overflows L2).  Each
+// stream still meets its query ranges in ring-replay order.
 struct QIter {
   const BaQRange* qr;
-  int rr, rrend, ti, sx, nstream;
+  int r0, rr, rrend, ti, sx, nstream;
   BaQRange cur;
-  __device__ void init(const BaQRange* q, int r0, int n, int ns) {
+  __device__ void init(const BaQRange* q, int first, int n, int ns) {
     qr = q;
-    rr = r0;
-    rrend = r0 + n;
+    r0 = first;
+    rr = first;
+    rrend = first + n;
     sx = 0;
     nstream = ns;
     if (rr < rrend) {
       cur = qr[rr];
       ti = cur.t0;
+    } else {
+      sx = ns;
     }
   }
-  __device__ bool valid() const { return rr < rrend; }
+  __device__ bool valid() const { return sx < nstream; }
   __device__ void next() {
-    if (++sx < nstream) return;
-    sx = 0;
     if (++ti < cur.t1) return;
     if (++rr < rrend) {
+      cur = qr[rr];
+      ti = cur.t0;
+      return;
+    }
+    if (++sx < nstream) {
+      rr = r0;
       cur = qr[rr];
       ti = cur.t0;
     }
   }
 };
-
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     main_bwd_kv_tc_kernel(const BaBwdArgs a, const __grid_constant__ CUtensorMap tmq,
