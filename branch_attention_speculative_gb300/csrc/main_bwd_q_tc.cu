@@ -270,11 +270,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive(bar(B_SEMPTY + sb));
         mbar_arrive(bar(B_DPEMPTY));
       }
+      if (climit >= KBN) {  // full block (the common case): no mask
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        const int c = half * 64 + e;
-        const float p = ex2_approx(fmaf(s[e], sh.scale_log2, -l2));
-        s[e] = (c < climit ? p : 0.f) * (dp[e] - delta);
+        for (int e = 0; e < 64; ++e) s[e] = ex2_approx(fmaf(s[e], sh.scale_log2, -l2)) * (dp[e] - delta);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const int c = half * 64 + e;
+          const float p = ex2_approx(fmaf(s[e], sh.scale_log2, -l2));
+          s[e] = (c < climit ? p : 0.f) * (dp[e] - delta);
+        }
       }
       // 64 keys = the eight 16-byte chunks of this row's line in block `half`
 #pragma unroll

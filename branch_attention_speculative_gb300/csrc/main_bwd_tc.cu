@@ -70,31 +70,40 @@ enum {
   B_COUNT = 14
 };
 
-// (stream, query range, query tile) iteration of one key tile.  The stream is
-// the outer loop: CTAs of neighbouring key tiles that run at the same time then
-// sweep the same stream's query tiles within a tile or two of each other, so
-// the Q / dO tiles they stream are shared in L2 (with the stream innermost the
-// shared window is ~28 tiles wide per CTA offset and overflows L2).  Each
-// stream still meets its query ranges in ring-replay order.
+// Iteration of one key tile over (phase, stream, query range, query tile).
+// Phase 0 covers the unmasked ranges (every range but the last when the last
+// is the diagonal one) for all streams, phase 1 the diagonal range for all
+// streams.  Key tiles of one sequence share the phase-0 sweep (same ranges, same
+// order), so CTAs that run at the same time read the same Q / dO tiles within a
+// tile or two of each other and share them in L2; the diagonal parts, whose
+// lengths differ, come last so they do not shift that sweep.
 struct QIter {
   const BaQRange* qr;
-  int r0, rr, rrend, ti, sx, nstream;
+  int first, nfull, nall, phase, rr, rrend, ti, sx, nstream;
   BaQRange cur;
-  __device__ void init(const BaQRange* q, int first, int n, int ns) {
+  __device__ void init(const BaQRange* q, int f, int n, int ns) {
     qr = q;
-    r0 = first;
-    rr = first;
-    rrend = first + n;
-    sx = 0;
+    first = f;
+    nall = n;
     nstream = ns;
-    if (rr < rrend) {
-      cur = qr[rr];
-      ti = cur.t0;
-    } else {
-      sx = ns;
+    nfull = (n > 0 && qr[f + n - 1].diag) ? n - 1 : n;
+    phase = 0;
+    sx = 0;
+    if (!start_phase()) {
+      phase = 1;
+      if (!start_phase()) phase = 2;
     }
   }
-  __device__ bool valid() const { return sx < nstream; }
+  // first range of the current phase for stream sx; false if the phase is empty
+  __device__ bool start_phase() {
+    rr = phase == 0 ? first : first + nfull;
+    rrend = phase == 0 ? first + nfull : first + nall;
+    if (rr >= rrend) return false;
+    cur = qr[rr];
+    ti = cur.t0;
+    return true;
+  }
+  __device__ bool valid() const { return phase < 2; }
   __device__ void next() {
     if (++ti < cur.t1) return;
     if (++rr < rrend) {
@@ -103,10 +112,12 @@ struct QIter {
       return;
     }
     if (++sx < nstream) {
-      rr = r0;
-      cur = qr[rr];
-      ti = cur.t0;
+      start_phase();
+      return;
     }
+    sx = 0;
+    if (++phase < 2 && start_phase()) return;
+    phase = 2;
   }
 };
 
@@ -278,12 +289,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // row records {lse*log2e, Delta, limit, 0}; queries past the tile are masked
       const float* rec = reinterpret_cast<const float*>(gbase + L::meta + qs * L::META) + 4 * col0;
       const int nq = qt.nrows - col0;
+      if (!diag && kok && nq >= 32) {
+        // full tile (the common case): no mask, one 8-byte load per column
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const bool v = kok && c < nq && (!diag || kpos <= __float_as_int(rec[4 * c + 2]));
-        const float p = ex2_approx(fmaf(s[c], sh.scale_log2, -rec[4 * c]));
-        s[c] = v ? p : 0.f;
-        dp[c] = s[c] * (dp[c] - rec[4 * c + 1]);
+        for (int c = 0; c < 32; ++c) {
+          const float2 r = *reinterpret_cast<const float2*>(rec + 4 * c);
+          const float p = ex2_approx(fmaf(s[c], sh.scale_log2, -r.x));
+          s[c] = p;
+          dp[c] = p * (dp[c] - r.y);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float4 r = *reinterpret_cast<const float4*>(rec + 4 * c);
+          const bool v = kok && c < nq && (!diag || kpos <= __float_as_int(r.z));
+          const float p = ex2_approx(fmaf(s[c], sh.scale_log2, -r.x));
+          s[c] = v ? p : 0.f;
+          dp[c] = s[c] * (dp[c] - r.y);
+        }
       }
       // P^T / dS^T are free once dV / dK of the previous pair have read them
       if (i >= 1 && !mbar_wait_warp(bar(B_PEMPTY), (i - 1) & 1, tb.status, abort_flag)) { ok = false; break; }

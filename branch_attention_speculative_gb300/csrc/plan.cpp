@@ -17,7 +17,8 @@
 // lists.  A forward query tile lists the key segments it visits in ring order
 // (chunk pairs above the diagonal are dropped, pairs below are unmasked, the
 // diagonal pair is cut at the tile's largest row limit); a backward key tile
-// lists the query-tile ranges that see it in ring-replay order.  Tiles are
+// lists the query-tile ranges that the ring replay brings to it (unmasked
+// chunks first in a canonical order, the diagonal chunk last).  Tiles are
 // handed out longest first.
 #include <algorithm>
 #include <atomic>
@@ -258,21 +259,24 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
       kt.chunk = gid;
       kt.qr0 = int32_t(p->bqr.size());
       kt.work = 0;
-      for (int step = 0; step < C; ++step) {
-        const int dst = (kch.rank + step) % C;
-        for (int qc : {dst, nch - 1 - dst}) {
-          const int32_t qg = kch.seq * nch + qc;
-          int32_t t0 = bfirst[qg], t1 = bfirst[qg] + bcount[qg];
-          int diag = 0;
-          if (qc < kch.c) continue;
-          if (qc == kch.c) {
-            while (t0 < t1 && p->bq[t0].lim_max < kt.pos0) ++t0;
-            diag = 1;
-          }
-          if (t0 >= t1) continue;
-          p->bqr.push_back(BaQRange{t0, t1, diag, 0});
-          kt.work += t1 - t0;
+      // The query chunks this key tile meets are those the ring replay brings
+      // to it (rank (r + s) mod C at step s): every later chunk of the
+      // sequence, unmasked, and its own chunk, cut by the causal limit.  They
+      // are listed unmasked chunks first, in descending chunk order — a prefix
+      // shared by every key tile of the sequence, so key tiles that run at the
+      // same time stream the same Q / dO tiles and share them in L2 — and the
+      // diagonal chunk last.  Only the summation order of dK / dV depends on it.
+      for (int qc = nch - 1; qc >= kch.c; --qc) {
+        const int32_t qg = kch.seq * nch + qc;
+        int32_t t0 = bfirst[qg], t1 = bfirst[qg] + bcount[qg];
+        int diag = 0;
+        if (qc == kch.c) {
+          while (t0 < t1 && p->bq[t0].lim_max < kt.pos0) ++t0;
+          diag = 1;
         }
+        if (t0 >= t1) continue;
+        p->bqr.push_back(BaQRange{t0, t1, diag, 0});
+        kt.work += t1 - t0;
       }
       kt.nqr = int32_t(p->bqr.size()) - kt.qr0;
       // kept even when no query sees it: its dK / dV must still be written (as zeros)
