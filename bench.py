@@ -234,12 +234,12 @@ def kernel_bytes(wl, info, name):
     d = wl.head_dim
     T = wl.tokens
     nbk = (wl.depth * T if wl.family == "ttt" else wl.num_anchors * wl.block) * wl.heads_kv
-    if name == "zigzag_pack":  # both passes pack q, k_m, v_m, k_b, v_b: read + write
-        return 2 * 2 * 2 * (R * d + 2 * T * wl.heads_kv * d + 2 * nbk * d)
+    if name == "zigzag_pack":  # one pass packing q, k_m, v_m, k_b, v_b: read + write
+        return 2 * 2 * (R * d + 2 * T * wl.heads_kv * d + 2 * nbk * d)
     if name == "lse_merge":
         return R * (2 * d * 4 + 2 * 4) + R * (d * 2 + 4)
-    if name == "bwd_prep":
-        return R * (2 * d * 2 + 4) + R * (d * 2 + 2 * 4 + d * 4)
+    if name == "bwd_prep":  # read o, dO, lse; write the row record and zero the dQ row
+        return R * (2 * d * 2 + 4) + R * (16 + d * 4)
     if name == "branch_fwd":
         return R * d * 2 + 2 * nbk * d * 2 + R * (d * 4 + 4)
     if name == "branch_bwd":

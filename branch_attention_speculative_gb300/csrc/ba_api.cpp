@@ -48,6 +48,7 @@ BaTables device_tables(const ba_plan* p, void* ws) {
   unsigned char* t = ws_at(ws, w.tables);
   BaTables tb{};
   tb.row_lim = reinterpret_cast<const int32_t*>(t + w.t_row_lim);
+  tb.nat_lim = reinterpret_cast<const int32_t*>(t + w.t_nat_lim);
   tb.tok_perm = reinterpret_cast<const int32_t*>(t + w.t_tok_perm);
   tb.anc_perm = reinterpret_cast<const int32_t*>(t + w.t_anc_perm);
   tb.fq = reinterpret_cast<const BaQTile*>(t + w.t_fq);
@@ -237,24 +238,17 @@ int ba_forward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, c
   BaFwdArgs a{};
   a.sh = p->shape;
   a.tb = device_tables(p, workspace);
-  a.qp = ws_at(workspace, w.qp);
-  a.kmp = ws_at(workspace, w.kmp);
-  a.vmp = ws_at(workspace, w.vmp);
-  a.kbp = ws_at(workspace, w.kbp);
-  a.vbp = ws_at(workspace, w.vbp);
+  a.q = q_b;
+  a.km = k_m;
+  a.vm = v_m;
+  a.kb = k_b;
+  a.vb = v_b;
   a.om = reinterpret_cast<float*>(ws_at(workspace, w.om));
   a.lm = reinterpret_cast<float*>(ws_at(workspace, w.lm));
   a.ob = reinterpret_cast<float*>(ws_at(workspace, w.ob));
   a.lb = reinterpret_cast<float*>(ws_at(workspace, w.lb));
   a.o = o;
   a.lse = lse;
-  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 0, q_b, const_cast<void*>(a.qp), 0, st); }));
-  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 1, k_m, const_cast<void*>(a.kmp), 0, st); }));
-  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 1, v_m, const_cast<void*>(a.vmp), 0, st); }));
-  if (has_b) {
-    BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, k_b, const_cast<void*>(a.kbp), 0, st); }));
-    BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, v_b, const_cast<void*>(a.vbp), 0, st); }));
-  }
   BA_TRY(timed(p, K_MAIN_FWD, st,
                [&] { return use_mma_fwd() ? ba_launch_main_fwd(a, st) : ba_launch_main_fwd_tc(a, st); }));
   if (has_b) BA_TRY(timed(p, K_BRANCH_FWD, st, [&] { return ba_launch_branch_fwd(a, st); }));
@@ -279,15 +273,14 @@ int ba_backward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, 
   BaBwdArgs a{};
   a.sh = p->shape;
   a.tb = device_tables(p, workspace);
-  a.qp = ws_at(workspace, w.qp);
-  a.kmp = ws_at(workspace, w.kmp);
-  a.vmp = ws_at(workspace, w.vmp);
-  a.kbp = ws_at(workspace, w.kbp);
-  a.vbp = ws_at(workspace, w.vbp);
+  a.q = q_b;
+  a.km = k_m;
+  a.vm = v_m;
+  a.kb = k_b;
+  a.vb = v_b;
   a.o = o;
   a.d_o = d_o;
   a.lse = lse;
-  a.dop = ws_at(workspace, w.dop);
   a.rowrec = reinterpret_cast<float4*>(ws_at(workspace, w.rowrec));
   a.dqacc = reinterpret_cast<float*>(ws_at(workspace, w.dqacc));
   a.dq = dq_b;
@@ -295,13 +288,6 @@ int ba_backward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, 
   a.dvm = dv_m;
   a.dkb = dk_b;
   a.dvb = dv_b;
-  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 0, q_b, const_cast<void*>(a.qp), 0, st); }));
-  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 1, k_m, const_cast<void*>(a.kmp), 0, st); }));
-  BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 1, v_m, const_cast<void*>(a.vmp), 0, st); }));
-  if (has_b) {
-    BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, k_b, const_cast<void*>(a.kbp), 0, st); }));
-    BA_TRY(timed(p, K_PACK, st, [&] { return pack(p, a.tb, 2, v_b, const_cast<void*>(a.vbp), 0, st); }));
-  }
   BA_TRY(timed(p, K_BWD_PREP, st, [&] { return ba_launch_bwd_prep(a, st); }));
   if (use_mma_bwd(a.sh)) {
     BA_TRY(timed(p, K_MAIN_BWD, st, [&] { return ba_launch_main_bwd(a, st); }));

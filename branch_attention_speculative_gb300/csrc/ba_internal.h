@@ -18,9 +18,13 @@
 #define BA_DEV_BOUNDS 2u
 
 // A run of <= BM consecutive packed query rows inside one zigzag chunk.  The
-// same tiling serves every query stream (step j and head h).
+// same tiling serves every query stream (step j and head h).  A chunk is a
+// contiguous range of natural positions (and of natural anchors), so the
+// tile's rows are also contiguous in the natural layout, from nrow0: kernels
+// address the caller's natural tensors directly (the zigzag pack is folded
+// into their load coordinates).
 struct BaQTile {
-  int32_t row0;     // first packed row (per stream)
+  int32_t row0;     // first packed row (per stream); indexes the row_lim table
   int32_t nrows;    // rows in the tile (<= BM)
   int32_t seg0;     // first key segment (forward) / unused (backward)
   int32_t nseg;     // key segments, in ring order
@@ -28,13 +32,16 @@ struct BaQTile {
   int32_t lim_max;  // largest row limit
   int32_t work;     // key blocks visited (forward) — used for longest-first order
   int32_t chunk;    // global chunk index (sequence * 2C + c)
+  int32_t nrow0;    // natural row (per stream) of row0; rows are contiguous
+  int32_t pad;
 };
 
 // A run of packed main keys inside one chunk that a query tile attends.
 struct BaKvSeg {
   int32_t k0;      // first packed key
   int32_t nkeys;   // keys in the segment
-  int32_t pos0;    // natural position of k0 (positions are contiguous inside a chunk)
+  int32_t pos0;    // natural position of k0 (positions are contiguous inside a
+                   // chunk): the key rows the kernels load
   int32_t diag;    // 1: the per-row causal limit cuts into the segment
 };
 
@@ -68,7 +75,8 @@ struct BaShape {
 
 // Device tables (inside the workspace).
 struct BaTables {
-  const int32_t* row_lim;   // [rows]
+  const int32_t* row_lim;   // [rows]   packed row -> last visible main position
+  const int32_t* nat_lim;   // [rows]   natural row -> last visible main position
   const int32_t* tok_perm;  // [T]   packed token -> natural token
   const int32_t* anc_perm;  // [NA]  packed anchor -> natural anchor (BLOCK)
   const BaQTile* fq;        // forward query tiles

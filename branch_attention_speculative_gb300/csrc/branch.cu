@@ -8,8 +8,8 @@
 //   TTT   — step-j query at anchor p sees branch keys (p, i), i <= j;
 //   BLOCK — each of the B queries of an anchor sees all B keys of the block.
 //
-// One CTA handles one anchor unit (a packed position for TTT, a packed anchor
-// for BLOCK) and one kv head: the unit's few branch keys are staged in shared
+// One CTA handles one anchor unit (a token position for TTT, an anchor for
+// BLOCK; natural order, since the branch part needs no zigzag) and one kv head: the unit's few branch keys are staged in shared
 // memory as fp32, each warp takes query rows, a lane owns d/32 columns, dot
 // products are warp-shuffle reductions.  The work is tiny next to the main
 // part and bound by HBM traffic of q, dO and the outputs.
@@ -28,17 +28,13 @@ __device__ __forceinline__ int rows_per_unit(const BaShape& sh) {
   return sh.family == BA_FAMILY_TTT ? sh.steps : (sh.family == BA_FAMILY_BLOCK ? sh.B : 1);
 }
 
-// packed branch-key slot of key i of unit u
+// branch-key slot of key i of unit u: TTT keys are [step, position],
+// BLOCK keys are [anchor, offset]
 __device__ __forceinline__ int64_t branch_slot(const BaShape& sh, int64_t u, int i) {
   return sh.family == BA_FAMILY_TTT ? int64_t(i) * sh.T + u : u * sh.B + i;
 }
 
-// natural branch-key slot of key i of packed unit u
-__device__ __forceinline__ int64_t branch_slot_nat(const BaShape& sh, const BaTables& tb, int64_t u, int i) {
-  return sh.family == BA_FAMILY_TTT ? int64_t(i) * sh.T + tb.tok_perm[u] : int64_t(tb.anc_perm[u]) * sh.B + i;
-}
-
-// (step j, packed row r) of query qi of unit u
+// (step j, row r) of query qi of unit u
 __device__ __forceinline__ void unit_query(const BaShape& sh, int64_t u, int qi, int64_t& j, int64_t& r) {
   if (sh.family == BA_FAMILY_TTT) { j = qi; r = u; }
   else if (sh.family == BA_FAMILY_BLOCK) { j = 0; r = u * sh.B + qi; }
@@ -95,9 +91,9 @@ __global__ void __launch_bounds__(128) branch_fwd_kernel(BaFwdArgs a) {
   float* ks = smem;
   float* vs = smem + sh.nbk * D;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const auto* qp = static_cast<const __nv_bfloat16*>(a.qp);
-  const auto* kb = static_cast<const __nv_bfloat16*>(a.kbp);
-  const auto* vb = static_cast<const __nv_bfloat16*>(a.vbp);
+  const auto* qg = static_cast<const __nv_bfloat16*>(a.q);
+  const auto* kb = static_cast<const __nv_bfloat16*>(a.kb);
+  const auto* vb = static_cast<const __nv_bfloat16*>(a.vb);
   const int64_t total = sh.units * sh.Hkv;
   const int nq = rows_per_unit(sh) * sh.G;
   for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
@@ -112,7 +108,7 @@ __global__ void __launch_bounds__(128) branch_fwd_kernel(BaFwdArgs a) {
       unit_query(sh, u, qi, j, r);
       const int64_t qrow = (j * sh.rows + r) * sh.Hq + kvh * sh.G + g;
       float q[E], acc[E];
-      load_row<D>(qp + qrow * D, lane, q);
+      load_row<D>(qg + qrow * D, lane, q);
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[e] = 0.f;
       float m = -INFINITY, l = 0.f;
@@ -149,10 +145,10 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
   float* dks = vs + sh.nbk * D;
   float* dvs = dks + sh.nbk * D;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const auto* qp = static_cast<const __nv_bfloat16*>(a.qp);
-  const auto* dop = static_cast<const __nv_bfloat16*>(a.dop);
-  const auto* kb = static_cast<const __nv_bfloat16*>(a.kbp);
-  const auto* vb = static_cast<const __nv_bfloat16*>(a.vbp);
+  const auto* qg = static_cast<const __nv_bfloat16*>(a.q);
+  const auto* dog = static_cast<const __nv_bfloat16*>(a.d_o);
+  const auto* kb = static_cast<const __nv_bfloat16*>(a.kb);
+  const auto* vb = static_cast<const __nv_bfloat16*>(a.vb);
   auto* dq = static_cast<__nv_bfloat16*>(a.dq);
   auto* dkb = static_cast<__nv_bfloat16*>(a.dkb);
   auto* dvb = static_cast<__nv_bfloat16*>(a.dvb);
@@ -173,8 +169,8 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
       unit_query(sh, u, qi, j, r);
       const int64_t qrow = (j * sh.rows + r) * sh.Hq + kvh * sh.G + g;
       float q[E], go[E], gq[E];
-      load_row<D>(qp + qrow * D, lane, q);
-      load_row<D>(dop + qrow * D, lane, go);
+      load_row<D>(qg + qrow * D, lane, q);
+      load_row<D>(dog + qrow * D, lane, go);
 #pragma unroll
       for (int e = 0; e < E; ++e) gq[e] = a.dqacc[qrow * D + lane * E + e];
       const int64_t srow = (j * sh.Hq + kvh * sh.G + g) * sh.rows + r;  // stream-major
@@ -200,13 +196,12 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
           atomicAdd(&dvs[i * D + lane * E + e], p * go[e]);
         }
       }
-      const int64_t nrow = (j * sh.rows + natural_row(sh, a.tb, r)) * sh.Hq + kvh * sh.G + g;
-      store_row_bf16<D>(dq + nrow * D, lane, gq);
+      store_row_bf16<D>(dq + qrow * D, lane, gq);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < sh.nbk * D; e += blockDim.x) {
       const int i = e / D, c = e % D;
-      const int64_t off = (branch_slot_nat(sh, a.tb, u, i) * sh.Hkv + kvh) * D + c;
+      const int64_t off = (branch_slot(sh, u, i) * sh.Hkv + kvh) * D + c;
       dkb[off] = __float2bfloat16_rn(dks[e]);
       dvb[off] = __float2bfloat16_rn(dvs[e]);
     }

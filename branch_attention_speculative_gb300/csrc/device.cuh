@@ -62,9 +62,3 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-
-// Natural index of a packed query row r of the per-stream row space.
-__device__ __forceinline__ int64_t natural_row(const BaShape& sh, const BaTables& tb, int64_t r) {
-  if (sh.family == BA_FAMILY_BLOCK) return int64_t(tb.anc_perm[r / sh.B]) * sh.B + (r % sh.B);
-  return tb.tok_perm[r];
-}

@@ -6,25 +6,26 @@
 
 #include "ba_internal.h"
 
+// All tensors are in the caller's natural layout: the kernels reach the zigzag
+// chunks through the plan's tile coordinates instead of packed copies.
 struct BaFwdArgs {
   BaShape sh;
   BaTables tb;
-  const void *qp, *kmp, *vmp, *kbp, *vbp;  // packed inputs (bf16)
-  float *om, *lm, *ob, *lb;                // packed partials (fp32)
-  void* o;                                 // natural output (bf16)
-  float* lse;                              // natural lse (fp32)
+  const void *q, *km, *vm, *kb, *vb;  // inputs (bf16)
+  float *om, *lm, *ob, *lb;           // main and branch partials (fp32, workspace)
+  void* o;                            // output (bf16)
+  float* lse;                         // lse (fp32)
 };
 
 struct BaBwdArgs {
   BaShape sh;
   BaTables tb;
-  const void *qp, *kmp, *vmp, *kbp, *vbp;  // packed inputs (bf16)
-  const void *o, *d_o;                     // natural (bf16)
-  const float* lse;                        // natural (fp32)
-  void* dop;                               // packed dO (bf16)
-  float4* rowrec;                          // per (step, head, row), stream-major: {lse*log2e, Delta, limit, 0}
-  float* dqacc;                            // packed dQ accumulator (fp32, like q_b)
-  void *dq, *dkm, *dvm, *dkb, *dvb;        // natural gradients (bf16)
+  const void *q, *km, *vm, *kb, *vb;  // inputs (bf16)
+  const void *o, *d_o;                // forward output and its gradient (bf16)
+  const float* lse;                   // forward lse (fp32)
+  float4* rowrec;                     // per (step, head, row), stream-major: {lse*log2e, Delta, limit, 0}
+  float* dqacc;                       // fp32 dQ accumulator, like q_b (workspace)
+  void *dq, *dkm, *dvm, *dkb, *dvb;   // gradients (bf16)
 };
 
 // K1: dst[o][i] = src[o][perm[i]] (inverse = 0) or dst[o][perm[i]] = src[o][i].
@@ -36,12 +37,12 @@ cudaError_t ba_launch_main_fwd_tc(const BaFwdArgs& a, cudaStream_t st);
 cudaError_t ba_launch_main_fwd(const BaFwdArgs& a, cudaStream_t st);
 // K3: rank-local branch attention -> O_b, l_b.
 cudaError_t ba_launch_branch_fwd(const BaFwdArgs& a, cudaStream_t st);
-// K4: Eq. 2 merge, packed partials -> natural o, lse.
+// K4: Eq. 2 merge of the partials -> o, lse.
 cudaError_t ba_launch_merge_plan(const BaFwdArgs& a, cudaStream_t st);
-// K4 on caller buffers with no permutation.
+// K4 on caller buffers.
 cudaError_t ba_launch_merge_rows(int64_t rows, int d, const float* om, const float* lm, const float* ob,
                                  const float* lb, void* o, float* l, cudaStream_t st);
-// K5: Delta = rowsum(dO * O), pack dO / lse, zero the dQ accumulator.
+// K5: Delta = rowsum(dO * O) and the row records; zeroes the dQ accumulator.
 cudaError_t ba_launch_bwd_prep(const BaBwdArgs& a, cudaStream_t st);
 // K6: main-attention backward (key-stationary): dK_m, dV_m (natural), dQ into the accumulator.
 // tcgen05 path (head_dim 128): key-stationary dK/dV kernel + query-stationary dQ

@@ -64,10 +64,10 @@ __global__ void __launch_bounds__(NT, 1) main_bwd_mma_kernel(BaBwdArgs a) {
   const BaKvTile kt = tb.bkv[tb.border[oi]];
   const int nstream = sh.steps * sh.G;
 
-  const auto* qp = static_cast<const __nv_bfloat16*>(a.qp);
-  const auto* dop = static_cast<const __nv_bfloat16*>(a.dop);
-  const auto* kmp = static_cast<const __nv_bfloat16*>(a.kmp);
-  const auto* vmp = static_cast<const __nv_bfloat16*>(a.vmp);
+  const auto* qg = static_cast<const __nv_bfloat16*>(a.q);
+  const auto* dog = static_cast<const __nv_bfloat16*>(a.d_o);
+  const auto* kmg = static_cast<const __nv_bfloat16*>(a.km);
+  const auto* vmg = static_cast<const __nv_bfloat16*>(a.vm);
   const int64_t kstride = int64_t(sh.Hkv) * D;
   const int64_t qstride = int64_t(sh.Hq) * D;
 
@@ -77,9 +77,9 @@ __global__ void __launch_bounds__(NT, 1) main_bwd_mma_kernel(BaBwdArgs a) {
   for (int c = tid; c < KB * CH; c += NT) {
     const int r = c / CH, col = (c % CH) * 8;
     const bool ok = r < kt.nkeys;
-    const int64_t key = int64_t(kt.k0) + (ok ? r : 0);
-    cp_async16(smem_u32(Ks + r * LD + col), kmp + key * kstride + int64_t(kvh) * D + col, ok ? 16 : 0);
-    cp_async16(smem_u32(Vs + r * LD + col), vmp + key * kstride + int64_t(kvh) * D + col, ok ? 16 : 0);
+    const int64_t key = int64_t(kt.pos0) + (ok ? r : 0);
+    cp_async16(smem_u32(Ks + r * LD + col), kmg + key * kstride + int64_t(kvh) * D + col, ok ? 16 : 0);
+    cp_async16(smem_u32(Vs + r * LD + col), vmg + key * kstride + int64_t(kvh) * D + col, ok ? 16 : 0);
   }
   cp_async_commit();
 
@@ -101,13 +101,13 @@ __global__ void __launch_bounds__(NT, 1) main_bwd_mma_kernel(BaBwdArgs a) {
     for (int c = tid; c < QB * CH; c += NT) {
       const int r = c / CH, col = (c % CH) * 8;
       const bool ok = r < qt.nrows;
-      const int64_t off = base + int64_t(qt.row0 + (ok ? r : 0)) * qstride + col;
-      cp_async16(smem_u32(qd + r * LD + col), qp + off, ok ? 16 : 0);
-      cp_async16(smem_u32(gd + r * LD + col), dop + off, ok ? 16 : 0);
+      const int64_t off = base + int64_t(qt.nrow0 + (ok ? r : 0)) * qstride + col;
+      cp_async16(smem_u32(qd + r * LD + col), qg + off, ok ? 16 : 0);
+      cp_async16(smem_u32(gd + r * LD + col), dog + off, ok ? 16 : 0);
     }
     for (int r = tid; r < QB; r += NT) {
       const bool ok = r < qt.nrows;
-      const int64_t srow = (int64_t(j) * sh.Hq + h) * sh.rows + qt.row0 + (ok ? r : 0);
+      const int64_t srow = (int64_t(j) * sh.Hq + h) * sh.rows + qt.nrow0 + (ok ? r : 0);
       const float4 rec = a.rowrec[srow];
       L2s[buf * QB + r] = ok ? rec.x : INFINITY;
       Dls[buf * QB + r] = ok ? rec.y : 0.f;
@@ -231,8 +231,8 @@ __global__ void __launch_bounds__(NT, 1) main_bwd_mma_kernel(BaBwdArgs a) {
     // dQ = dS K: warp w takes query rows 16(w % 4).. and d-half w / 4
     const int qw = warp & 3, half = warp >> 2;
     const int qA = qw * 16 + g, qB = qA + 8;
-    const int64_t rowA = (int64_t(j) * sh.rows + qt.row0 + qA) * sh.Hq + h;
-    const int64_t rowB = (int64_t(j) * sh.rows + qt.row0 + qB) * sh.Hq + h;
+    const int64_t rowA = (int64_t(j) * sh.rows + qt.nrow0 + qA) * sh.Hq + h;
+    const int64_t rowB = (int64_t(j) * sh.rows + qt.nrow0 + qB) * sh.Hq + h;
     {
       float dq[D / 16][4];
 #pragma unroll
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(NT, 1) main_bwd_mma_kernel(BaBwdArgs a) {
   auto* dkm = static_cast<__nv_bfloat16*>(a.dkm);
   auto* dvm = static_cast<__nv_bfloat16*>(a.dvm);
   if (kokA) {
-    const int64_t base = (int64_t(tb.tok_perm[kt.k0 + kA]) * sh.Hkv + kvh) * D;
+    const int64_t base = (int64_t(kt.pos0 + kA) * sh.Hkv + kvh) * D;
 #pragma unroll
     for (int dt = 0; dt < D / 8; ++dt) {
       const int col = dt * 8 + 2 * t4;
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(NT, 1) main_bwd_mma_kernel(BaBwdArgs a) {
     }
   }
   if (kokB) {
-    const int64_t base = (int64_t(tb.tok_perm[kt.k0 + kB]) * sh.Hkv + kvh) * D;
+    const int64_t base = (int64_t(kt.pos0 + kB) * sh.Hkv + kvh) * D;
 #pragma unroll
     for (int dt = 0; dt < D / 8; ++dt) {
       const int col = dt * 8 + 2 * t4;

@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&tmdo);
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
-      const int qrow = int(int64_t(j) * sh.rows + tile.row0);
+      const int qrow = int(int64_t(j) * sh.rows + tile.nrow0);
       mbar_expect_tx(bar(B_QFULL), 4 * L::TILE);
       for (int cb = 0; cb < 2; ++cb) {
         tma_load_3d(sbase + L::q + cb * L::TILE, &tmq, bar(B_QFULL), cb * 64, h, qrow);
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int i = 0; it.valid(); ++i, it.next()) {
         const int st = i & 1;
         const uint32_t ph = (i >> 1) & 1;
-        const int key = it.cur.k0 + it.kb;
+        const int key = it.cur.pos0 + it.kb;  // natural key row
         if (!mbar_wait(bar(B_KEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
         mbar_expect_tx(bar(B_KFULL + st), 2 * L::TILE);
         for (int cb = 0; cb < 2; ++cb)
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float l2 = 0.f, delta = 0.f;
     int lim = -1;
     if (rok) {
-      const float4 rec = a.rowrec[(int64_t(j) * sh.Hq + h) * sh.rows + tile.row0 + r];
+      const float4 rec = a.rowrec[(int64_t(j) * sh.Hq + h) * sh.rows + tile.nrow0 + r];
       l2 = rec.x;
       delta = rec.y;
       lim = __float_as_int(rec.z);
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // each warp writes d-columns 64 (w / 4) .. of its 32 rows
     if (ok && i > 0 && mbar_wait_warp(bar(B_DSEMPTY), (i - 1) & 1, tb.status, abort_flag)) {
       tc_fence_after();
-      const int64_t qrow = (int64_t(j) * sh.rows + tile.row0 + r) * sh.Hq + h;
+      const int64_t qrow = (int64_t(j) * sh.rows + tile.nrow0 + r) * sh.Hq + h;
       float4* dst = reinterpret_cast<float4*>(a.dqacc + qrow * D + half * 64);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -358,10 +358,10 @@ cudaError_t ba_launch_main_bwd_q_tc(const BaBwdArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int64_t qrows = int64_t(a.sh.steps) * a.sh.rows;
   CUtensorMap mq, mdo, mk, mv;
-  if ((e = map3d(&mq, a.qp, a.sh.Hq, qrows)) != cudaSuccess) return e;
-  if ((e = map3d(&mdo, a.dop, a.sh.Hq, qrows)) != cudaSuccess) return e;
-  if ((e = map3d(&mk, a.kmp, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
-  if ((e = map3d(&mv, a.vmp, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  if ((e = map3d(&mq, a.q, a.sh.Hq, qrows)) != cudaSuccess) return e;
+  if ((e = map3d(&mdo, a.d_o, a.sh.Hq, qrows)) != cudaSuccess) return e;
+  if ((e = map3d(&mk, a.km, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  if ((e = map3d(&mv, a.vm, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
   const int smem = int(DqSmem::alloc);
   if ((e = cudaFuncSetAttribute(main_bwd_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
       cudaSuccess)

@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (any) {
         mbar_expect_tx(bar(B_KV), 4 * L::KT);
         for (int cb = 0; cb < 2; ++cb) {
-          tma_load_3d(sbase + L::k + cb * L::KT, &tmk, bar(B_KV), cb * 64, kvh, kt.k0);
-          tma_load_3d(sbase + L::v + cb * L::KT, &tmv, bar(B_KV), cb * 64, kvh, kt.k0);
+          tma_load_3d(sbase + L::k + cb * L::KT, &tmk, bar(B_KV), cb * 64, kvh, kt.pos0);
+          tma_load_3d(sbase + L::v + cb * L::KT, &tmv, bar(B_KV), cb * 64, kvh, kt.pos0);
         }
       }
     }
@@ -201,8 +201,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(bar(B_QEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
         const BaQTile qt = tb.bq[it.ti];
         const int j = it.sx / sh.G, h = kvh * sh.G + it.sx % sh.G;
-        const int qrow = int(int64_t(j) * sh.rows + qt.row0);
-        const int srow = int((int64_t(j) * sh.Hq + h) * sh.rows + qt.row0);
+        const int qrow = int(int64_t(j) * sh.rows + qt.nrow0);
+        const int srow = int((int64_t(j) * sh.Hq + h) * sh.rows + qt.nrow0);
         mbar_expect_tx(bar(B_QFULL + st), 4 * L::QT + L::META);
         for (int cb = 0; cb < 2; ++cb) {
           tma_load_3d(sbase + L::q + (st * 2 + cb) * L::QT, &tmq, bar(B_QFULL + st), cb * 64, h, qrow);
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto* dvm = static_cast<__nv_bfloat16*>(a.dvm);
     const bool have = any && ok && i > 0 && mbar_wait_warp(bar(B_DONE), 0, tb.status, abort_flag);
     if (have) tc_fence_after();
-    const int64_t base = kok ? (int64_t(tb.tok_perm[kt.k0 + row]) * sh.Hkv + kvh) * D + half * 64 : 0;
+    const int64_t base = kok ? (int64_t(kt.pos0 + row) * sh.Hkv + kvh) * D + half * 64 : 0;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       float xk[32], xv[32];
@@ -409,12 +409,12 @@ cudaError_t ba_launch_main_bwd_kv_tc(const BaBwdArgs& a, cudaStream_t st) {
   const int64_t qrows = int64_t(a.sh.steps) * a.sh.rows;
   CUtensorMap mq, mdo, mk, mv;
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if ((e = map3d(&mq, a.qp, bf, 2, 128, a.sh.Hq, qrows, 64, QBM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
-  if ((e = map3d(&mdo, a.dop, bf, 2, 128, a.sh.Hq, qrows, 64, QBM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+  if ((e = map3d(&mq, a.q, bf, 2, 128, a.sh.Hq, qrows, 64, QBM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+  if ((e = map3d(&mdo, a.d_o, bf, 2, 128, a.sh.Hq, qrows, 64, QBM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
-  if ((e = map3d(&mk, a.kmp, bf, 2, 128, a.sh.Hkv, a.sh.T, 64, KBN, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+  if ((e = map3d(&mk, a.km, bf, 2, 128, a.sh.Hkv, a.sh.T, 64, KBN, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
-  if ((e = map3d(&mv, a.vmp, bf, 2, 128, a.sh.Hkv, a.sh.T, 64, KBN, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+  if ((e = map3d(&mv, a.vm, bf, 2, 128, a.sh.Hkv, a.sh.T, 64, KBN, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
   CUtensorMap mrec;
   {

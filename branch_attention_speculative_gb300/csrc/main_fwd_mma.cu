@@ -44,14 +44,14 @@ __global__ void __launch_bounds__(256, 1) main_fwd_mma_kernel(BaFwdArgs a) {
   const int j = rem / sh.G;
   const int h = kvh * sh.G + rem % sh.G;
 
-  const auto* qp = static_cast<const __nv_bfloat16*>(a.qp);
-  const auto* kmp = static_cast<const __nv_bfloat16*>(a.kmp);
-  const auto* vmp = static_cast<const __nv_bfloat16*>(a.vmp);
+  const auto* qg = static_cast<const __nv_bfloat16*>(a.q);
+  const auto* kmg = static_cast<const __nv_bfloat16*>(a.km);
+  const auto* vmg = static_cast<const __nv_bfloat16*>(a.vm);
   const int64_t qstride = int64_t(sh.Hq) * D;
-  const __nv_bfloat16* qbase = qp + (int64_t(j) * sh.rows * sh.Hq + h) * D;
+  const __nv_bfloat16* qbase = qg + (int64_t(j) * sh.rows * sh.Hq + h) * D;
   const int64_t kstride = int64_t(sh.Hkv) * D;
-  const __nv_bfloat16* kbase = kmp + int64_t(kvh) * D;
-  const __nv_bfloat16* vbase = vmp + int64_t(kvh) * D;
+  const __nv_bfloat16* kbase = kmg + int64_t(kvh) * D;
+  const __nv_bfloat16* vbase = vmg + int64_t(kvh) * D;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(256, 1) main_fwd_mma_kernel(BaFwdArgs a) {
   for (int c = tid; c < FBM * CH; c += 256) {
     const int r = c / CH, col = (c % CH) * 8;
     const bool ok = r < tile.nrows;
-    const __nv_bfloat16* src = qbase + int64_t(tile.row0 + (ok ? r : 0)) * qstride + col;
+    const __nv_bfloat16* src = qbase + int64_t(tile.nrow0 + (ok ? r : 0)) * qstride + col;
     cp_async16(smem_u32(Qs + r * LD + col), src, ok ? 16 : 0);
   }
   cp_async_commit();
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256, 1) main_fwd_mma_kernel(BaFwdArgs a) {
     for (int c = tid; c < FBN * CH; c += 256) {
       const int r = c / CH, col = (c % CH) * 8;
       const bool ok = kb + r < sg.nkeys;
-      const int64_t key = int64_t(sg.k0) + (ok ? kb + r : 0);
+      const int64_t key = int64_t(sg.pos0) + (ok ? kb + r : 0);
       cp_async16(smem_u32(kd + r * LD + col), kbase + key * kstride + col, ok ? 16 : 0);
       cp_async16(smem_u32(vd + r * LD + col), vbase + key * kstride + col, ok ? 16 : 0);
     }
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(256, 1) main_fwd_mma_kernel(BaFwdArgs a) {
   lA += __shfl_xor_sync(0xffffffffu, lA, 2);
   lB += __shfl_xor_sync(0xffffffffu, lB, 1);
   lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-  const int64_t rowbase = int64_t(j) * sh.rows + tile.row0;
+  const int64_t rowbase = int64_t(j) * sh.rows + tile.nrow0;
   if (rA < tile.nrows) {
     const int64_t qrow = (rowbase + rA) * sh.Hq + h;
     const float inv = lA > 0.f ? 1.f / lA : 0.f;

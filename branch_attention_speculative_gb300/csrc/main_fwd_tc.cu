@@ -152,13 +152,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&tmv);
       mbar_expect_tx(bar(B_QFULL), CB * L::TILE);
       for (int cb = 0; cb < CB; ++cb)
-        tma_load_3d(sbase + L::q + cb * L::TILE, &tmq, bar(B_QFULL), cb * 64, h, int(j * sh.rows + tile.row0));
+        tma_load_3d(sbase + L::q + cb * L::TILE, &tmq, bar(B_QFULL), cb * 64, h, int(j * sh.rows + tile.nrow0));
       BlockIter it;
       it.init(tb.fseg, tile.seg0, tile.nseg);
       for (int i = 0; it.valid(); ++i, it.next()) {
         const int st = i & 1;
         const uint32_t ph = (i >> 1) & 1;
-        const int key = it.cur.k0 + it.kb;
+        const int key = it.cur.pos0 + it.kb;  // natural key row
         if (!mbar_wait(bar(B_KEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
         mbar_expect_tx(bar(B_KFULL + st), CB * L::TILE);
         for (int cb = 0; cb < CB; ++cb)
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && i > 0 && mbar_wait_warp(bar(B_ODONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, tb.status, abort_flag)) {
       tc_fence_after();
       const bool write = r < tile.nrows;
-      const int64_t qrow = (int64_t(j) * sh.rows + tile.row0 + r) * sh.Hq + h;
+      const int64_t qrow = (int64_t(j) * sh.rows + tile.nrow0 + r) * sh.Hq + h;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float4* dst = reinterpret_cast<float4*>(a.om + qrow * D);
 #pragma unroll
@@ -369,9 +369,9 @@ template <int D>
 cudaError_t launch(const BaFwdArgs& a, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   cudaError_t e;
-  if ((e = make_map(&mq, a.qp, D, a.sh.Hq, int64_t(a.sh.steps) * a.sh.rows)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.kmp, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.vmp, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  if ((e = make_map(&mq, a.q, D, a.sh.Hq, int64_t(a.sh.steps) * a.sh.rows)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.km, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.vm, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
   const int64_t grid = int64_t(a.tb.n_fq) * a.sh.steps * a.sh.Hq;
   const int smem = int(FwdSmem<D>::alloc);
   if ((e = cudaFuncSetAttribute(main_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=

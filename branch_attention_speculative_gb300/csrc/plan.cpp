@@ -181,6 +181,18 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
     }
   }
 
+  // natural row -> limit (TTT / causal: the row's own position; block: its anchor)
+  p->nat_lim.assign(rows, 0);
+  if (fam != BA_FAMILY_BLOCK) {
+    for (int64_t r = 0; r < T; ++r) p->nat_lim[r] = int32_t(r);
+  } else {
+    for (int64_t a = 0; a < NA; ++a)
+      for (int u = 0; u < B; ++u) p->nat_lim[a * B + u] = p->anchors[a];
+  }
+  auto natural_row = [&](int32_t r) -> int32_t {
+    return fam == BA_FAMILY_BLOCK ? p->anc_perm[r / B] * B + r % B : p->tok_perm[r];
+  };
+
   // ---- useful pairs
   p->main_pairs = 0;
   for (const BaChunk& ch : p->chunks) {
@@ -207,6 +219,7 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
         t.lim_min = p->row_lim[r0];
         t.lim_max = p->row_lim[r0 + t.nrows - 1];
         t.chunk = gid;
+        t.nrow0 = natural_row(r0);
         out.push_back(t);
       }
       if (count) (*count)[gid] = int32_t(out.size()) - (*first)[gid];
@@ -304,6 +317,7 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
   w.tables = off;
   size_t t = 0;
   w.t_row_lim = t; t += table_span(p->row_lim);
+  w.t_nat_lim = t; t += table_span(p->nat_lim);
   w.t_tok_perm = t; t += table_span(p->tok_perm);
   w.t_anc_perm = t; t += table_span(p->anc_perm);
   w.t_fq = t; t += table_span(p->fq);
@@ -316,13 +330,11 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
   w.table_bytes = t;
   off += t;
   const size_t qrows = size_t(sh.steps) * size_t(rows) * size_t(sh.Hq);
-  const size_t nbk_total = fam == BA_FAMILY_TTT ? size_t(D) * T : (fam == BA_FAMILY_BLOCK ? size_t(NA) * B : 0);
   const size_t dd = size_t(sh.d);
-  w.qp = off; off = align256(off + qrows * dd * 2);
-  w.kmp = off; off = align256(off + size_t(T) * sh.Hkv * dd * 2);
-  w.vmp = off; off = align256(off + size_t(T) * sh.Hkv * dd * 2);
-  w.kbp = off; off = align256(off + nbk_total * sh.Hkv * dd * 2);
-  w.vbp = off; off = align256(off + nbk_total * sh.Hkv * dd * 2);
+  // The kernels read the caller's natural-layout tensors directly, so the
+  // workspace holds only partials: forward O_m, l_m (and O_b, l_b with
+  // branches), backward row records and the fp32 dQ accumulator.  The two
+  // regions overlap.
   const size_t scratch = off;
   size_t f = scratch;
   w.om = f; f = align256(f + qrows * dd * 4);
@@ -330,7 +342,6 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
   w.ob = f; f = align256(f + (fam == BA_FAMILY_CAUSAL ? 0 : qrows * dd * 4));
   w.lb = f; f = align256(f + (fam == BA_FAMILY_CAUSAL ? 0 : qrows * 4));
   size_t b = scratch;
-  w.dop = b; b = align256(b + qrows * dd * 2);
   w.rowrec = b; b = align256(b + qrows * 16);
   w.dqacc = b; b = align256(b + qrows * dd * 4);
   w.total = std::max(f, b);
@@ -342,6 +353,7 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
     return BA_ERR_HOST_ALLOC;
   }
   put(p->image, w.t_row_lim, p->row_lim);
+  put(p->image, w.t_nat_lim, p->nat_lim);
   put(p->image, w.t_tok_perm, p->tok_perm);
   put(p->image, w.t_anc_perm, p->anc_perm);
   put(p->image, w.t_fq, p->fq);
@@ -374,9 +386,20 @@ int ba_validate_plan(const ba_plan* p) {
   }
   for (int32_t v : p->row_lim)
     if (v < 0 || v >= T) return bad();
+  if (int64_t(p->nat_lim.size()) != rows) return bad();
+  auto natural_row = [&](int32_t r) -> int64_t {
+    return sh.family == BA_FAMILY_BLOCK ? int64_t(p->anc_perm[r / sh.B]) * sh.B + r % sh.B : p->tok_perm[r];
+  };
   auto check_tile = [&](const BaQTile& t, int bm) {
-    return t.row0 >= 0 && t.nrows >= 1 && t.nrows <= bm && int64_t(t.row0) + t.nrows <= rows &&
-           t.lim_min <= t.lim_max && p->row_lim[t.row0] == t.lim_min && p->row_lim[t.row0 + t.nrows - 1] == t.lim_max;
+    if (!(t.row0 >= 0 && t.nrows >= 1 && t.nrows <= bm && int64_t(t.row0) + t.nrows <= rows &&
+          t.lim_min <= t.lim_max && p->row_lim[t.row0] == t.lim_min && p->row_lim[t.row0 + t.nrows - 1] == t.lim_max))
+      return false;
+    // rows are contiguous in the natural layout and keep their limits there
+    for (int32_t i = 0; i < t.nrows; ++i) {
+      const int64_t nr = natural_row(t.row0 + i);
+      if (nr != int64_t(t.nrow0) + i || p->nat_lim[nr] != p->row_lim[t.row0 + i]) return false;
+    }
+    return true;
   };
   for (const BaQTile& t : p->fq) {
     if (!check_tile(t, BA_FWD_BM) || t.seg0 < 0 || t.nseg < 1 || int64_t(t.seg0) + t.nseg > int64_t(p->fseg.size()))

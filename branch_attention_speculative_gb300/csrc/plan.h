@@ -14,10 +14,9 @@ struct BaWorkspaceLayout {
   size_t status;                  // device status word (256 B)
   size_t tables;                  // start of the uploaded table image
   size_t table_bytes;             // size of the table image
-  size_t t_row_lim, t_tok_perm, t_anc_perm, t_fq, t_fseg, t_forder, t_bq, t_bkv, t_bqr, t_border;
-  size_t qp, kmp, vmp, kbp, vbp;  // zigzag-packed inputs (bf16)
-  size_t om, lm, ob, lb;          // forward partials (fp32)
-  size_t dop, rowrec, dqacc;      // backward scratch: packed dO (bf16), row records (16 B), dQ (fp32)
+  size_t t_row_lim, t_nat_lim, t_tok_perm, t_anc_perm, t_fq, t_fseg, t_forder, t_bq, t_bkv, t_bqr, t_border;
+  size_t om, lm, ob, lb;          // forward partials (fp32, natural order)
+  size_t rowrec, dqacc;           // backward scratch: row records (16 B), dQ (fp32), natural order
   size_t total;
 };
 
@@ -41,7 +40,7 @@ struct ba_plan {
   int64_t NA;
 
   std::vector<BaChunk> chunks;   // indexed seq * 2C + c
-  std::vector<int32_t> row_lim, tok_perm, anc_perm, tok_rank;
+  std::vector<int32_t> row_lim, nat_lim, tok_perm, anc_perm, tok_rank;
   std::vector<BaQTile> fq;
   std::vector<BaKvSeg> fseg;
   std::vector<int32_t> forder;

@@ -1,11 +1,11 @@
 // K5 — backward preprocessing.
 //
 // For every query-head row: Delta = <dO, O> in fp32 (the row term of the
-// softmax backward, dS = P * (dP - Delta)); dO and lse are gathered into the
-// packed zigzag order the main backward reads; lse (in base 2), Delta and the
-// row's key limit go into one 16-byte record per (step, head, row), stored
-// stream-major so that a query tile's records are one contiguous TMA box; the
-// row of the fp32 dQ accumulator is zeroed.  The pages only say that the backward replays the
+// softmax backward, dS = P * (dP - Delta)).  lse (in base 2), Delta and the
+// row's main-key limit go into one 16-byte record per (step, head, row), in
+// natural row order and stream-major, so that the records of a query tile (a
+// run of consecutive natural rows) are one contiguous TMA box; the row of the
+// fp32 dQ accumulator is zeroed.  The pages only say that the backward replays the
 // ring ("Online Draft Co-Training ...", rainbus page, method step 5); Delta is
 // what that replay needs per row when P is recomputed from the merged lse.
 // HBM-bound: d/8 threads per row, 16-byte loads.
@@ -23,7 +23,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BaBwdArgs a) {
   const int64_t rows = int64_t(sh.steps) * sh.rows * sh.Hq;
   const auto* o = static_cast<const uint4*>(a.o);
   const auto* go = static_cast<const uint4*>(a.d_o);
-  auto* dop = static_cast<uint4*>(a.dop);
   // block-uniform trip count: the shuffles below need every lane of the warp
   for (int64_t base = int64_t(blockIdx.x) * RPB; base < rows; base += int64_t(gridDim.x) * RPB) {
     const int64_t row = base + threadIdx.x / TPR;
@@ -32,11 +31,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BaBwdArgs a) {
     const int64_t jr = row / sh.Hq;
     const int64_t j = jr / sh.rows;
     const int64_t r = jr - j * sh.rows;
-    const int64_t nrow = valid ? (j * sh.rows + natural_row(sh, a.tb, r)) * sh.Hq + h : 0;
     uint4 ov = make_uint4(0, 0, 0, 0), gv = make_uint4(0, 0, 0, 0);
     if (valid) {
-      ov = o[nrow * TPR + sub];
-      gv = go[nrow * TPR + sub];
+      ov = o[row * TPR + sub];
+      gv = go[row * TPR + sub];
     }
     float acc = 0.f;
     const uint32_t* ow = reinterpret_cast<const uint32_t*>(&ov);
@@ -49,13 +47,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BaBwdArgs a) {
 #pragma unroll
     for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
     if (!valid) continue;
-    dop[row * TPR + sub] = gv;
     float4* dq = reinterpret_cast<float4*>(a.dqacc + row * D);
     dq[2 * sub] = make_float4(0.f, 0.f, 0.f, 0.f);
     dq[2 * sub + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (sub == 0) {  // one 16-byte record per (step, head, row), stream-major
       const int64_t srow = (j * sh.Hq + h) * sh.rows + r;
-      a.rowrec[srow] = make_float4(a.lse[nrow] * BA_LOG2E, acc, __int_as_float(a.tb.row_lim[r]), 0.f);
+      a.rowrec[srow] = make_float4(a.lse[row] * BA_LOG2E, acc, __int_as_float(a.tb.nat_lim[r]), 0.f);
     }
   }
 }
