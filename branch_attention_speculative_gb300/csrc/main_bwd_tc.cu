@@ -13,17 +13,28 @@
 //   S^T  = K Q^T        M=128 keys, N=64 queries, K=d        -> TMEM (2 buffers)
 //   dP^T = V dO^T       same                                  -> TMEM (2 buffers)
 //   (threads)  P^T = exp2(S^T * scale*log2e - lse*log2e),  dS^T = P^T (dP^T - Delta)
-//              written as bf16 into 128B-swizzled shared tiles [key][query]
-//   dV  += P^T dO       M=128 keys, N=d, K=64 queries (dO as an MN-major operand)
-//   dK  += dS^T Q       same
+//              written back as bf16 into the S^T buffer they came from
+//   dV  += P^T dO       M=128 keys, N=d, K=64 queries; P^T read from TMEM,
+//                       dO an MN-major shared operand
+//   dK  += dS^T Q       same, dS^T from TMEM
 // dK and dV stay in TMEM for the whole CTA and are written once, in natural
 // order, at the end.  dQ is computed by the query-stationary kernel
-// (main_bwd_q_tc.cu), which needs no atomics.  TMEM: S^T buffers [0,64) and
-// [64,128), dP^T buffers [128,192) and [192,256), dK [256,384), dV [384,512).
+// (main_bwd_q_tc.cu), which needs no atomics.
+// TMEM columns: three S^T buffers [0,64) [64,128) [128,192), one dP^T buffer
+// [192,256), dK [256,384), dV [384,512).  An S^T buffer stays busy from its
+// S^T GEMM until the dV/dK GEMMs of the same pair have read P^T / dS^T out of
+// it; the dP^T buffer is free as soon as the threads have loaded it.  With
+// three S^T buffers the S^T/dP^T GEMMs of the next pair are always queued
+// behind the dV/dK GEMMs of the current one, and the threads' exp work on a
+// pair overlaps the tensor cores' work on its neighbours.
+// Inside an S^T buffer the compute warp of query half h (queries 32h..32h+31)
+// reads fp32 columns [32h, 32h+32) and writes back, into the same columns,
+// P^T (bf16 pairs) at [32h, 32h+16) and dS^T at [32h+16, 32h+32); no warp
+// writes a column another warp still has to read.
 // Warp roles: warps 0-7 compute (warp w: TMEM lane quarter w % 4 = key rows,
 // query columns 32 (w / 4) ..; two warps per SM sub-partition hide each
 // other's latencies), warp 8 loads with TMA (Q, dO and the tile's 16-byte row
-// records {lse*log2e, Delta, key limit}) into a 3-stage ring, warp 9 issues the
+// records {lse*log2e, Delta, key limit}) into a 4-stage ring, warp 9 issues the
 // MMAs and owns TMEM.  All waits are bounded.
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -39,7 +50,8 @@ constexpr int KBN = 128;  // keys per CTA
 constexpr int QBM = 64;   // queries per tile
 constexpr int NTHREADS = 320;  // 8 compute warps, 1 TMA warp, 1 MMA warp
 
-constexpr int NQS = 3;    // query-tile pipeline stages
+constexpr int NQS = 4;    // query-tile pipeline stages
+constexpr int NSB = 3;    // S^T buffers in TMEM
 
 struct BwdSmem {
   static constexpr uint32_t KT = 128u * 128u;  // [128 keys][64 d] bf16 block
@@ -50,25 +62,25 @@ struct BwdSmem {
   static constexpr uint32_t q = v + 2 * KT;    // [NQS stages][2 blocks]
   static constexpr uint32_t go = q + NQS * 2 * QT;
   static constexpr uint32_t meta = go + NQS * 2 * QT;  // [NQS stages]
-  // P^T then dS^T, [128 keys][64 queries] bf16 each
-  static constexpr uint32_t pt = meta + NQS * META;
-  static constexpr uint32_t dst = pt + KT;
-  static constexpr uint32_t bars = dst + KT;
+  static constexpr uint32_t bars = meta + NQS * META;
   static constexpr uint32_t bytes = bars + 256;
   static constexpr uint32_t alloc = bytes + 1024;
 };
 
 enum {
   B_KV = 0,
-  B_QFULL = 1,   // [NQS]
-  B_QEMPTY = 4,  // [NQS]
-  B_SFULL = 7,   // [2]
-  B_SEMPTY = 9,  // [2]
-  B_PFULL = 11,
-  B_PEMPTY = 12,
-  B_DONE = 13,
-  B_COUNT = 14
+  B_QFULL = 1,                 // [NQS]
+  B_QEMPTY = B_QFULL + NQS,    // [NQS]
+  B_SFULL = B_QEMPTY + NQS,    // [NSB] S^T and dP^T of a pair are in TMEM
+  B_SEMPTY = B_SFULL + NSB,    // [NSB] dV/dK of the pair have read the buffer
+  B_DPEMPTY = B_SEMPTY + NSB,  // the threads have loaded dP^T
+  B_PFULL = B_DPEMPTY + 1,     // [NSB] P^T and dS^T are in TMEM (one barrier per
+                               // buffer: the threads can finish a pair before the
+                               // MMA warp has waited for the previous one)
+  B_DONE = B_PFULL + NSB,
+  B_COUNT = B_DONE + 1
 };
+static_assert(8 * B_COUNT + 16 <= 256, "barrier area");
 
 // Iteration of one key tile over (phase, stream, query range, query tile).
 // Phase 0 covers the unmasked ranges (every range but the last when the last
@@ -156,12 +168,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_QFULL + s), 1);
       mbar_init(bar(B_QEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NSB; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SEMPTY + s), 8);
+      mbar_init(bar(B_SEMPTY + s), 1);
+      mbar_init(bar(B_PFULL + s), 8);
     }
-    mbar_init(bar(B_PFULL), 8);
-    mbar_init(bar(B_PEMPTY), 1);
+    mbar_init(bar(B_DPEMPTY), 8);
     mbar_init(bar(B_DONE), 1);
     fence_mbar_init();
   }
@@ -173,7 +185,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tDP = tmem + 128, tDK = tmem + 256, tDV = tmem + 384;
+  const uint32_t tS = tmem, tDP = tmem + 192, tDK = tmem + 256, tDV = tmem + 384;
   const bool any = kt.nqr > 0;
 
   if (warp == 8) {
@@ -220,9 +232,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int r = kt.qr0; r < kt.qr0 + kt.nqr; ++r) n += (tb.bqr[r].t1 - tb.bqr[r].t0) * nstream;
       auto issue_sdp = [&](int i) -> bool {
         const int qs = i % NQS;
-        const int sb = i & 1;
+        const int sb = i % NSB;
         if (!mbar_wait(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) return false;
-        if (!mbar_wait(bar(B_SEMPTY + sb), ((i >> 1) & 1) ^ 1, tb.status, abort_flag)) return false;
+        if (!mbar_wait(bar(B_SEMPTY + sb), ((i / NSB) & 1) ^ 1, tb.status, abort_flag)) return false;
+        if (!mbar_wait(bar(B_DPEMPTY), (i & 1) ^ 1, tb.status, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -230,7 +243,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t oq = (kk >> 2) * L::QT + (kk & 3) * 32;
           tc_mma(tS + sb * 64, smem_desc_sw128(sbase + L::k + ok_, 16, 1024),
                  smem_desc_sw128(sbase + L::q + qs * 2 * L::QT + oq, 16, 1024), id_s, kk > 0);
-          tc_mma(tDP + sb * 64, smem_desc_sw128(sbase + L::v + ok_, 16, 1024),
+          tc_mma(tDP, smem_desc_sw128(sbase + L::v + ok_, 16, 1024),
                  smem_desc_sw128(sbase + L::go + qs * 2 * L::QT + oq, 16, 1024), id_s, kk > 0);
         }
         tc_commit(bar(B_SFULL + sb));
@@ -240,18 +253,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (ok && n > 0) ok = issue_sdp(0);
       for (int i = 0; ok && i < n; ++i) {
         if (i + 1 < n && !issue_sdp(i + 1)) break;
-        if (!mbar_wait(bar(B_PFULL), i & 1, tb.status, abort_flag)) break;
+        if (!mbar_wait(bar(B_PFULL + i % NSB), (i / NSB) & 1, tb.status, abort_flag)) break;
         tc_fence_after();
         const int qs = i % NQS;
         const uint32_t qb = sbase + L::q + qs * 2 * L::QT, gb = sbase + L::go + qs * 2 * L::QT;
+        const uint32_t pa = tS + (i % NSB) * 64;
 #pragma unroll
         for (int kk = 0; kk < QBM / 16; ++kk) {
-          tc_mma(tDV, smem_desc_sw128(sbase + L::pt + kk * 32, 16, 1024),
-                 smem_desc_sw128(gb + kk * 2048, L::QT, 1024), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-          tc_mma(tDK, smem_desc_sw128(sbase + L::dst + kk * 32, 16, 1024),
-                 smem_desc_sw128(qb + kk * 2048, L::QT, 1024), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+          // queries 16 kk .. 16 kk + 15 sit in query half kk / 2 of the buffer
+          const uint32_t col = (kk >> 1) * 32 + (kk & 1) * 8;
+          tc_mma_tmem_a(tDV, pa + col, smem_desc_sw128(gb + kk * 2048, L::QT, 1024), id_kv,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_tmem_a(tDK, pa + col + 16, smem_desc_sw128(qb + kk * 2048, L::QT, 1024), id_kv,
+                        (i > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(bar(B_PEMPTY));
+        tc_commit(bar(B_SEMPTY + i % NSB));
         tc_commit(bar(B_QEMPTY + qs));
       }
       tc_commit(bar(B_DONE));
@@ -271,8 +287,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bool ok = true;
     int i = 0;
     for (; it.valid(); ++i, it.next()) {
-      const int qs = i % NQS, sb = i & 1;
-      const uint32_t ph = (i >> 1) & 1;
+      const int qs = i % NQS, sb = i % NSB;
+      const uint32_t ph = (i / NSB) & 1;
       const BaQTile qt = tb.bq[it.ti];
       const bool diag = it.cur.diag != 0;
       // q_full: the row records of this tile are in shared memory
@@ -281,11 +297,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       float s[32], dp[32];
       tmem_ld32(tS + lane_off + sb * 64 + col0, s);
-      tmem_ld32(tDP + lane_off + sb * 64 + col0, dp);
+      tmem_ld32(tDP + lane_off + col0, dp);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SEMPTY + sb));  // S^T / dP^T buffers are free again
+      if (lane == 0) mbar_arrive(bar(B_DPEMPTY));  // the dP^T buffer is free again
       // row records {lse*log2e, Delta, limit, 0}; queries past the tile are masked
       const float* rec = reinterpret_cast<const float*>(gbase + L::meta + qs * L::META) + 4 * col0;
       const int nq = qt.nrows - col0;
@@ -308,25 +324,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           dp[c] = s[c] * (dp[c] - r.y);
         }
       }
-      // P^T / dS^T are free once dV / dK of the previous pair have read them
-      if (i >= 1 && !mbar_wait_warp(bar(B_PEMPTY), (i - 1) & 1, tb.status, abort_flag)) { ok = false; break; }
-      const uint32_t rowoff = (row >> 3) * 1024 + (row & 7) * 128;
+      // P^T and dS^T back into this warp's own columns of the S^T buffer
+      uint32_t pw[16], dw[16];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint32_t sw = (((half * 4 + q4) ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(sbase + L::pt + rowoff + sw),
-                     "r"(pack_bf16(s[8 * q4], s[8 * q4 + 1])), "r"(pack_bf16(s[8 * q4 + 2], s[8 * q4 + 3])),
-                     "r"(pack_bf16(s[8 * q4 + 4], s[8 * q4 + 5])), "r"(pack_bf16(s[8 * q4 + 6], s[8 * q4 + 7]))
-                     : "memory");
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(sbase + L::dst + rowoff + sw),
-                     "r"(pack_bf16(dp[8 * q4], dp[8 * q4 + 1])), "r"(pack_bf16(dp[8 * q4 + 2], dp[8 * q4 + 3])),
-                     "r"(pack_bf16(dp[8 * q4 + 4], dp[8 * q4 + 5])), "r"(pack_bf16(dp[8 * q4 + 6], dp[8 * q4 + 7]))
-                     : "memory");
+      for (int e = 0; e < 16; ++e) {
+        pw[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
+        dw[e] = pack_bf16(dp[2 * e], dp[2 * e + 1]);
       }
-      fence_proxy_async_smem();
+      tmem_st16(tS + lane_off + sb * 64 + col0, pw);
+      tmem_st16(tS + lane_off + sb * 64 + col0 + 16, dw);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL));
+      if (lane == 0) mbar_arrive(bar(B_PFULL + sb));
     }
     // epilogue: dK (scaled) and dV of this key tile, natural order; each warp
     // writes d-columns 64 (w / 4) .. 64 (w / 4) + 63 of its 32 key rows
