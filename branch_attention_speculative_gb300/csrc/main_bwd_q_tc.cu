@@ -7,16 +7,24 @@
 // key segments the planner lists for it in ring order.  P is recomputed from
 // the merged lse (exact for both key sets, since the merged result is the
 // single softmax over their union), so no running max is needed:
-//   S  = Q K^T          M=128 queries, N=128 keys, K=d        -> TMEM (2 buffers)
-//   dP = dO V^T         same                                  -> TMEM
+//   dP = dO V^T         M=128 queries, N=128 keys, K=d        -> TMEM
+//   S  = Q K^T          same                                  -> TMEM (2 buffers)
 //   (threads)  P = exp2(S * scale*log2e - lse*log2e) with the causal / ragged
-//              mask, dS = P (dP - Delta), written as bf16 into a 128B-swizzled
-//              shared tile [query][key]
-//   dQ += dS K          M=128 queries, N=d, K=128 keys (K read MN-major) -> TMEM
+//              mask, dS = P (dP - Delta), written back as bf16 into the S
+//              buffer it came from
+//   dQ += dS K          M=128 queries, N=d, K=128 keys; dS read from TMEM as
+//                       the A operand, K an MN-major shared operand -> TMEM
 // dQ stays in TMEM for the whole tile and is written once, scaled, into the
 // fp32 dQ accumulator (no atomics, no read-modify-write); the branch backward
 // adds the branch part and writes the bf16 result.
-// TMEM: S0 [0,128), S1 [128,256), dP [256,384), dQ [384,512).
+// TMEM: S0 [0,128), S1 [128,256), dP [256,384), dQ [384,512).  Inside an S
+// buffer the warp of key half h reads fp32 columns [64h, 64h+64) and writes
+// dS (bf16 pairs) back into [64h, 64h+32): no warp writes a column another
+// warp still has to read.  The MMA warp issues dP(i+1), S(i+1), dQ(i) in that
+// order: S(i+1) reuses the buffer dQ(i-1) read, and dP(i+1) covers the wait
+// for dQ(i-1) to finish, so the tensor cores never drain between blocks.
+// K sits in a three-stage ring (it is read by S and, a block later, by dQ), V
+// in a two-stage ring.
 // Warps: 0-7 compute (warp w: TMEM lane quarter w % 4 = query rows, keys
 // 64 (w / 4) .. of each block; two warps per SM sub-partition hide each other's
 // latencies), 8 TMA, 9 MMA + TMEM.
@@ -33,33 +41,35 @@ namespace {
 constexpr int QBM = 128;  // query rows per tile (BA_FWD_BM)
 constexpr int KBN = 128;  // keys per block
 constexpr int NTHREADS = 320;  // 8 compute warps, 1 TMA warp, 1 MMA warp
+constexpr int NK = 3;          // K ring stages
+constexpr int NV = 2;          // V ring stages
 
 struct DqSmem {
   static constexpr uint32_t TILE = 128u * 128u;  // [128 rows][64 columns] bf16, swizzled
   static constexpr uint32_t q = 0;               // 2 blocks
   static constexpr uint32_t go = q + 2 * TILE;   // 2 blocks
-  static constexpr uint32_t k = go + 2 * TILE;   // [2 stages][2 blocks]
-  static constexpr uint32_t v = k + 4 * TILE;    // [2 stages][2 blocks]
-  static constexpr uint32_t ds = v + 4 * TILE;   // dS [128 queries][128 keys]: 2 blocks
-  static constexpr uint32_t bars = ds + 2 * TILE;
+  static constexpr uint32_t k = go + 2 * TILE;       // [NK stages][2 blocks]
+  static constexpr uint32_t v = k + NK * 2 * TILE;   // [NV stages][2 blocks]
+  static constexpr uint32_t bars = v + NV * 2 * TILE;
   static constexpr uint32_t bytes = bars + 256;
   static constexpr uint32_t alloc = bytes + 1024;
 };
 
 enum {
   B_QFULL = 0,
-  B_KFULL = 1,    // [2]
-  B_KEMPTY = 3,   // [2]
-  B_VFULL = 5,    // [2]
-  B_VEMPTY = 7,   // [2]
-  B_SFULL = 9,    // [2]
-  B_SEMPTY = 11,  // [2]
-  B_DPFULL = 13,
-  B_DPEMPTY = 14,
-  B_DSFULL = 15,
-  B_DSEMPTY = 16,
-  B_COUNT = 17
+  B_KFULL = 1,                // [NK]
+  B_KEMPTY = B_KFULL + NK,    // [NK]
+  B_VFULL = B_KEMPTY + NK,    // [NV]
+  B_VEMPTY = B_VFULL + NV,    // [NV]
+  B_SFULL = B_VEMPTY + NV,    // [2] dP and S of a block are in TMEM
+  B_DSFULL = B_SFULL + 2,     // [2] dS of a block is in TMEM (per buffer, so the
+                              // threads can finish a block before the MMA warp
+                              // has waited for the previous one)
+  B_SFREE = B_DSFULL + 2,     // [2] dQ of the block is done: the buffer is free
+  B_DPEMPTY = B_SFREE + 2,    // the threads have loaded dP
+  B_COUNT = B_DPEMPTY + 1
 };
+static_assert(8 * B_COUNT + 16 <= 256, "barrier area");
 
 struct BlockIter {
   const BaKvSeg* seg;
@@ -118,18 +128,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(bar(B_QFULL), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NK; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
-      mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SEMPTY + s), 8);
     }
-    mbar_init(bar(B_DPFULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_DSFULL + s), 8);
+      mbar_init(bar(B_SFREE + s), 1);
+    }
     mbar_init(bar(B_DPEMPTY), 8);
-    mbar_init(bar(B_DSFULL), 8);
-    mbar_init(bar(B_DSEMPTY), 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -158,17 +170,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       BlockIter it;
       it.init(tb.fseg, tile.seg0, tile.nseg);
       for (int i = 0; it.valid(); ++i, it.next()) {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
+        const int ks = i % NK, vs = i % NV;
         const int key = it.cur.pos0 + it.kb;  // natural key row
-        if (!mbar_wait(bar(B_KEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
-        mbar_expect_tx(bar(B_KFULL + st), 2 * L::TILE);
+        if (!mbar_wait(bar(B_VEMPTY + vs), ((i / NV) & 1) ^ 1, tb.status, abort_flag)) break;
+        mbar_expect_tx(bar(B_VFULL + vs), 2 * L::TILE);
         for (int cb = 0; cb < 2; ++cb)
-          tma_load_3d(sbase + L::k + (st * 2 + cb) * L::TILE, &tmk, bar(B_KFULL + st), cb * 64, kvh, key);
-        if (!mbar_wait(bar(B_VEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
-        mbar_expect_tx(bar(B_VFULL + st), 2 * L::TILE);
+          tma_load_3d(sbase + L::v + (vs * 2 + cb) * L::TILE, &tmv, bar(B_VFULL + vs), cb * 64, kvh, key);
+        if (!mbar_wait(bar(B_KEMPTY + ks), ((i / NK) & 1) ^ 1, tb.status, abort_flag)) break;
+        mbar_expect_tx(bar(B_KFULL + ks), 2 * L::TILE);
         for (int cb = 0; cb < 2; ++cb)
-          tma_load_3d(sbase + L::v + (st * 2 + cb) * L::TILE, &tmv, bar(B_VFULL + st), cb * 64, kvh, key);
+          tma_load_3d(sbase + L::k + (ks * 2 + cb) * L::TILE, &tmk, bar(B_KFULL + ks), cb * 64, kvh, key);
       }
     }
   } else if (warp == 9) {
@@ -176,54 +187,58 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (elect_one()) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, KBN, false, false);  // S, dP
       constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);     // dQ (K as MN-major B)
-      auto issue_s_dp = [&](int i) -> bool {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait(bar(B_KFULL + st), ph, tb.status, abort_flag)) return false;
-        if (!mbar_wait(bar(B_SEMPTY + st), ph ^ 1, tb.status, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
-          tc_mma(tS + st * KBN, smem_desc_sw128(sbase + L::q + off, 16, 1024),
-                 smem_desc_sw128(sbase + L::k + st * 2 * L::TILE + off, 16, 1024), id_s, kk > 0);
-        }
-        tc_commit(bar(B_SFULL + st));
-        if (!mbar_wait(bar(B_VFULL + st), ph, tb.status, abort_flag)) return false;
+      auto issue_dp = [&](int i) -> bool {
+        const int vs = i % NV;
+        if (!mbar_wait(bar(B_VFULL + vs), (i / NV) & 1, tb.status, abort_flag)) return false;
         if (!mbar_wait(bar(B_DPEMPTY), (i & 1) ^ 1, tb.status, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
           tc_mma(tDP, smem_desc_sw128(sbase + L::go + off, 16, 1024),
-                 smem_desc_sw128(sbase + L::v + st * 2 * L::TILE + off, 16, 1024), id_s, kk > 0);
+                 smem_desc_sw128(sbase + L::v + vs * 2 * L::TILE + off, 16, 1024), id_s, kk > 0);
         }
-        tc_commit(bar(B_DPFULL));
-        tc_commit(bar(B_VEMPTY + st));
+        tc_commit(bar(B_VEMPTY + vs));
+        return true;
+      };
+      auto issue_s = [&](int i) -> bool {
+        const int ks = i % NK, sb = i & 1;
+        if (!mbar_wait(bar(B_KFULL + ks), (i / NK) & 1, tb.status, abort_flag)) return false;
+        if (!mbar_wait(bar(B_SFREE + sb), ((i >> 1) & 1) ^ 1, tb.status, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
+          tc_mma(tS + sb * KBN, smem_desc_sw128(sbase + L::q + off, 16, 1024),
+                 smem_desc_sw128(sbase + L::k + ks * 2 * L::TILE + off, 16, 1024), id_s, kk > 0);
+        }
+        tc_commit(bar(B_SFULL + sb));  // also covers dP(i), issued before
         return true;
       };
       auto issue_dq = [&](int i) -> bool {
-        const int st = i & 1;
-        if (!mbar_wait(bar(B_DSFULL), i & 1, tb.status, abort_flag)) return false;
+        const int ks = i % NK, sb = i & 1;
+        if (!mbar_wait(bar(B_DSFULL + sb), (i >> 1) & 1, tb.status, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t kbase = sbase + L::k + st * 2 * L::TILE;
+        const uint32_t kbase = sbase + L::k + ks * 2 * L::TILE;
 #pragma unroll
         for (int kk = 0; kk < KBN / 16; ++kk)
-          tc_mma(tDQ, smem_desc_sw128(sbase + L::ds + (kk >> 2) * L::TILE + (kk & 3) * 32, 16, 1024),
-                 smem_desc_sw128(kbase + kk * 2048, L::TILE, 1024), id_q, (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(B_DSEMPTY));
-        tc_commit(bar(B_KEMPTY + st));
+          tc_mma_tmem_a(tDQ, tS + sb * KBN + (kk >> 2) * 64 + (kk & 3) * 8,
+                        smem_desc_sw128(kbase + kk * 2048, L::TILE, 1024), id_q, (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(B_SFREE + sb));
+        tc_commit(bar(B_KEMPTY + ks));
         return true;
       };
       bool ok = mbar_wait(bar(B_QFULL), 0, tb.status, abort_flag);
-      BlockIter it;
-      it.init(tb.fseg, tile.seg0, tile.nseg);
-      int i = 0;
-      for (; ok && it.valid(); ++i, it.next()) {
-        if (!issue_s_dp(i)) { ok = false; break; }
-        if (i > 0 && !issue_dq(i - 1)) { ok = false; break; }
+      int n = 0;  // blocks, counted the way the other roles walk them
+      {
+        BlockIter it;
+        for (it.init(tb.fseg, tile.seg0, tile.nseg); it.valid(); it.next()) ++n;
       }
-      if (ok && i > 0) issue_dq(i - 1);
+      if (ok && n > 0) ok = issue_dp(0) && issue_s(0);
+      for (int i = 0; ok && i < n; ++i) {
+        if (i + 1 < n && !(issue_dp(i + 1) && issue_s(i + 1))) break;
+        if (!issue_dq(i)) break;
+      }
     }
   } else {
     // ------------------------------------------------------------ compute
@@ -251,11 +266,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int nvalid = it.cur.nkeys - it.kb;
       const int climit = !rok ? 0 : (it.cur.diag ? min(nvalid, lim - (it.cur.pos0 + it.kb) + 1) : nvalid);
       if (!mbar_wait_warp(bar(B_SFULL + sb), ph, tb.status, abort_flag)) { ok = false; break; }
-      if (!mbar_wait_warp(bar(B_DPFULL), i & 1, tb.status, abort_flag)) { ok = false; break; }
-      // the dS tile was last read by dQ(i - 1)
-      if (i >= 1 && !mbar_wait_warp(bar(B_DSEMPTY), (i - 1) & 1, tb.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t drow = sbase + L::ds + (r >> 3) * 1024 + (r & 7) * 128;
       // this warp's 64 keys: both S and dP chunks loaded before one wait
       float s[64], dp[64];
       tmem_ld32(tS + lane_off + sb * KBN + half * 64, s);
@@ -263,13 +274,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_ld32(tDP + lane_off + half * 64, dp);
       tmem_ld32(tDP + lane_off + half * 64 + 32, dp + 32);
       tmem_wait_ld();
-      // S and dP are in registers: their TMEM buffers can be refilled now
+      // dP is in registers: its TMEM buffer can be refilled now
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(B_SEMPTY + sb));
-        mbar_arrive(bar(B_DPEMPTY));
-      }
+      if (lane == 0) mbar_arrive(bar(B_DPEMPTY));
       if (climit >= KBN) {  // full block (the common case): no mask
 #pragma unroll
         for (int e = 0; e < 64; ++e) s[e] = ex2_approx(fmaf(s[e], sh.scale_log2, -l2)) * (dp[e] - delta);
@@ -281,22 +289,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           s[e] = (c < climit ? p : 0.f) * (dp[e] - delta);
         }
       }
-      // 64 keys = the eight 16-byte chunks of this row's line in block `half`
+      // dS (bf16, keys 2c and 2c + 1 of this half in column c) back into the
+      // first 32 of this warp's 64 columns of the S buffer
+      {
+        uint32_t w[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = drow + half * L::TILE + (((c ^ (r & 7))) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
-                     "r"(pack_bf16(s[8 * c], s[8 * c + 1])), "r"(pack_bf16(s[8 * c + 2], s[8 * c + 3])),
-                     "r"(pack_bf16(s[8 * c + 4], s[8 * c + 5])), "r"(pack_bf16(s[8 * c + 6], s[8 * c + 7]))
-                     : "memory");
+        for (int e = 0; e < 32; ++e) w[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
+        tmem_st32u(tS + lane_off + sb * KBN + half * 64, w);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DSFULL));
+      if (lane == 0) mbar_arrive(bar(B_DSFULL + sb));
     }
     // epilogue: dQ (main part, scaled) -> fp32 accumulator row, written once;
     // each warp writes d-columns 64 (w / 4) .. of its 32 rows
-    if (ok && i > 0 && mbar_wait_warp(bar(B_DSEMPTY), (i - 1) & 1, tb.status, abort_flag)) {
+    if (ok && i > 0 && mbar_wait_warp(bar(B_SFREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, tb.status, abort_flag)) {
       tc_fence_after();
       const int64_t qrow = (int64_t(j) * sh.rows + tile.nrow0 + r) * sh.Hq + h;
       float4* dst = reinterpret_cast<float4*>(a.dqacc + qrow * D + half * 64);

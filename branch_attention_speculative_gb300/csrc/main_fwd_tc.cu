@@ -13,14 +13,19 @@
 // against blocks of 128 keys of kv head h / G.  Warp roles:
 //   warps 0-3  softmax: thread t owns row t (TMEM lane t).  Reads S from TMEM,
 //              masks the ragged block end and the per-row causal limit on the
-//              diagonal chunk, keeps the row max / sum, writes P (bf16) into a
-//              128B-swizzled shared tile, rescales O in TMEM only when the row
-//              max grew by more than 2^8 (the values of P stay below 256), and
-//              finally writes O_m = O / l and l_m.
-//   warp 4     TMA producer: Q once, then K and V blocks into two-stage rings.
-//   warp 5     MMA issuer (one thread): S = Q K^T into one of two TMEM S
-//              buffers, then O += P V for the previous block; owns TMEM.
-// TMEM: S0 = columns [0,128), S1 = [128,256), O = [256, 256 + d).
+//              diagonal chunk, keeps the row max / sum, writes P (bf16, two
+//              per 32-bit column) back into the first 64 columns of the same
+//              S buffer, rescales O in TMEM only when the row max grew by more
+//              than 2^8 (the values of P stay below 256), and finally writes
+//              O_m = O / l and l_m.
+//   warp 4     TMA producer: Q once, then K and V blocks into three-stage rings.
+//   warp 5     MMA issuer (one thread): S = Q K^T into one of three TMEM S
+//              buffers, then O += P V for the previous block with P read from
+//              TMEM as the A operand; owns TMEM.
+// TMEM: S buffers at columns [0,128), [128,256), [256,384); O = [384, 384 + d).
+// An S buffer is busy from its QK^T GEMM until the PV GEMM of the same block
+// has read P out of it, so with three of them the next block's QK^T is always
+// queued on the tensor cores behind the current PV while the softmax runs.
 // Every wait is bounded (BA_WAIT_CYCLES); a timeout records BA_DEV_TIMEOUT,
 // every role leaves its loop, and TMEM is released before the CTA exits.
 #include <cudaTypedefs.h>
@@ -36,16 +41,17 @@ namespace {
 constexpr int TBM = 128;  // query rows per tile
 constexpr int TBN = 128;  // keys per block
 constexpr int NTHREADS = 192;
+constexpr int NKV = 3;    // K / V ring stages
+constexpr int NSB = 3;    // S (and P) buffers in TMEM
 
 template <int D>
 struct FwdSmem {
   static constexpr int CB = D / 64;                       // 64-column (128-byte) blocks per row
   static constexpr uint32_t TILE = 128u * 128u;           // one 128-row x 128-byte swizzled block
   static constexpr uint32_t q = 0;
-  static constexpr uint32_t k = q + CB * TILE;            // [2 stages][CB blocks]
-  static constexpr uint32_t v = k + 2 * CB * TILE;        // [2 stages][CB blocks]
-  static constexpr uint32_t p = v + 2 * CB * TILE;        // [2 buffers][2 blocks of 64 keys]
-  static constexpr uint32_t bars = p + 2 * 2 * TILE;
+  static constexpr uint32_t k = q + CB * TILE;            // [NKV stages][CB blocks]
+  static constexpr uint32_t v = k + NKV * CB * TILE;      // [NKV stages][CB blocks]
+  static constexpr uint32_t bars = v + NKV * CB * TILE;
   static constexpr uint32_t bytes = bars + 256;
   static constexpr uint32_t alloc = bytes + 1024;         // slack for 1024-byte alignment
 };
@@ -53,16 +59,18 @@ struct FwdSmem {
 // barrier slots (8 bytes each) after FwdSmem::bars
 enum {
   B_QFULL = 0,
-  B_KFULL = 1,   // [2]
-  B_KEMPTY = 3,  // [2]
-  B_VFULL = 5,   // [2]
-  B_VEMPTY = 7,  // [2]
-  B_SFULL = 9,   // [2]
-  B_SEMPTY = 11, // [2]
-  B_PFULL = 13,  // [2]
-  B_ODONE = 15,  // [2]
-  B_COUNT = 17
+  B_KFULL = 1,                // [NKV]
+  B_KEMPTY = B_KFULL + NKV,   // [NKV]
+  B_VFULL = B_KEMPTY + NKV,   // [NKV]
+  B_VEMPTY = B_VFULL + NKV,   // [NKV]
+  B_SFULL = B_VEMPTY + NKV,   // [NSB] S of a block is in TMEM
+  B_PFULL = B_SFULL + NSB,    // [NSB] P of a block is in TMEM (per buffer, so the
+                              // softmax can run a block ahead of the MMA warp's wait)
+  B_SFREE = B_PFULL + NSB,    // [NSB] the block's PV GEMM is done: O is up to date
+                              // and the S / P buffer is free
+  B_COUNT = B_SFREE + NSB
 };
+static_assert(8 * B_COUNT + 16 <= 256, "barrier area");
 
 struct BlockIter {
   const BaKvSeg* seg;
@@ -122,15 +130,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(bar(B_QFULL), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NKV; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
+    }
+    for (int s = 0; s < NSB; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SEMPTY + s), 4);
       mbar_init(bar(B_PFULL + s), 4);
-      mbar_init(bar(B_ODONE + s), 1);
+      mbar_init(bar(B_SFREE + s), 1);
     }
     fence_mbar_init();
   }
@@ -142,7 +151,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 256;
+  const uint32_t tS = tmem, tO = tmem + NSB * TBN;
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
@@ -156,8 +165,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       BlockIter it;
       it.init(tb.fseg, tile.seg0, tile.nseg);
       for (int i = 0; it.valid(); ++i, it.next()) {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
+        const int st = i % NKV;
+        const uint32_t ph = (i / NKV) & 1;
         const int key = it.cur.pos0 + it.kb;  // natural key row
         if (!mbar_wait(bar(B_KEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
         mbar_expect_tx(bar(B_KFULL + st), CB * L::TILE);
@@ -175,21 +184,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, TBN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
       auto issue_pv = [&](int i) -> bool {
-        const int pb = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait(bar(B_PFULL + pb), ph, tb.status, abort_flag)) return false;
-        if (!mbar_wait(bar(B_VFULL + pb), ph, tb.status, abort_flag)) return false;
+        const int pb = i % NSB, vs = i % NKV;
+        if (!mbar_wait(bar(B_PFULL + pb), (i / NSB) & 1, tb.status, abort_flag)) return false;
+        if (!mbar_wait(bar(B_VFULL + vs), (i / NKV) & 1, tb.status, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t pbase = sbase + L::p + pb * 2 * L::TILE;
-        const uint32_t vbase = sbase + L::v + pb * CB * L::TILE;
+        const uint32_t vbase = sbase + L::v + vs * CB * L::TILE;
 #pragma unroll
         for (int kk = 0; kk < TBN / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(pbase + (kk >> 2) * L::TILE + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, L::TILE, 1024);
-          tc_mma(tO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_tmem_a(tO, tS + pb * TBN + kk * 8, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(bar(B_ODONE + pb));
-        tc_commit(bar(B_VEMPTY + pb));
+        tc_commit(bar(B_SFREE + pb));
+        tc_commit(bar(B_VEMPTY + vs));
         return true;
       };
       bool ok = mbar_wait(bar(B_QFULL), 0, tb.status, abort_flag);
@@ -197,20 +203,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       it.init(tb.fseg, tile.seg0, tile.nseg);
       int i = 0;
       for (; ok && it.valid(); ++i, it.next()) {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait(bar(B_KFULL + st), ph, tb.status, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(bar(B_SEMPTY + st), ph ^ 1, tb.status, abort_flag)) { ok = false; break; }
+        const int ks = i % NKV, sb = i % NSB;
+        if (!mbar_wait(bar(B_KFULL + ks), (i / NKV) & 1, tb.status, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(bar(B_SFREE + sb), ((i / NSB) & 1) ^ 1, tb.status, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kbase = sbase + L::k + st * CB * L::TILE;
+        const uint32_t kbase = sbase + L::k + ks * CB * L::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
-          tc_mma(tS + st * TBN, smem_desc_sw128(sbase + L::q + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024),
+          tc_mma(tS + sb * TBN, smem_desc_sw128(sbase + L::q + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024),
                  idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar(B_SFULL + st));
-        tc_commit(bar(B_KEMPTY + st));
+        tc_commit(bar(B_SFULL + sb));
+        tc_commit(bar(B_KEMPTY + ks));
         if (i > 0 && !issue_pv(i - 1)) { ok = false; break; }
       }
       if (ok && i > 0) issue_pv(i - 1);
@@ -226,17 +231,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int i = 0;
     bool ok = true;
     for (; it.valid(); ++i, it.next()) {
-      const int sb = i & 1;
-      const uint32_t ph = (i >> 1) & 1;
+      const int sb = i % NSB;
+      const uint32_t ph = (i / NSB) & 1;
       if (!mbar_wait_warp(bar(B_SFULL + sb), ph, tb.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
       float s[TBN];
 #pragma unroll
       for (int c = 0; c < TBN / 32; ++c) tmem_ld32(tS + lane_off + sb * TBN + c * 32, s + c * 32);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SEMPTY + sb));
       // mask: ragged end of the segment, causal limit on the diagonal chunk
       const int nvalid = it.cur.nkeys - it.kb;
       if (it.cur.diag || nvalid < TBN) {
@@ -265,15 +267,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         rsp[c & 7] += s[c];
       }
       const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
-      // the P buffer was last read by PV(i - 2)
-      if (i >= 2 && !mbar_wait_warp(bar(B_ODONE + sb), ((i - 2) >> 1) & 1, tb.status, abort_flag)) {
-        ok = false;
-        break;
-      }
-      // rescale O (warp-uniform TMEM access) when any row's max grew
+      // rescale O (warp-uniform TMEM access) when any row's max grew; PV of
+      // the previous block must have landed first
       if (i >= 1 && __any_sync(0xffffffffu, grow)) {
-        const int pb = (i - 1) & 1;
-        if (!mbar_wait_warp(bar(B_ODONE + pb), ((i - 1) >> 1) & 1, tb.status, abort_flag)) { ok = false; break; }
+        const int pb = (i - 1) % NSB;
+        if (!mbar_wait_warp(bar(B_SFREE + pb), ((i - 1) / NSB) & 1, tb.status, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const float cfac = grow ? ex2_approx(m_used - base) : 1.f;
 #pragma unroll
@@ -292,25 +290,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       m_used = m_next;
       l += rs;
-      // P (bf16) -> swizzled K-major tile: row r, keys 8c..8c+7 in 16-byte chunk c
-      const uint32_t prow = sbase + L::p + sb * 2 * L::TILE + (r >> 3) * 1024 + (r & 7) * 128;
+      // P (bf16, keys 2c and 2c + 1 in column c) back into this row's lane of
+      // the S buffer; only this thread reads or writes the lane
 #pragma unroll
-      for (int c = 0; c < TBN / 8; ++c) {
-        const uint32_t addr = prow + (c >> 3) * L::TILE + (((c & 7) ^ (r & 7)) << 4);
-        const uint32_t w0 = pack_bf16(s[8 * c + 0], s[8 * c + 1]);
-        const uint32_t w1 = pack_bf16(s[8 * c + 2], s[8 * c + 3]);
-        const uint32_t w2 = pack_bf16(s[8 * c + 4], s[8 * c + 5]);
-        const uint32_t w3 = pack_bf16(s[8 * c + 6], s[8 * c + 7]);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
-                     : "memory");
+      for (int h2 = 0; h2 < TBN / 64; ++h2) {
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) w[e] = pack_bf16(s[64 * h2 + 2 * e], s[64 * h2 + 2 * e + 1]);
+        tmem_st32u(tS + lane_off + sb * TBN + h2 * 32, w);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL + sb));
     }
     // epilogue: O / l and the natural-log lse of the main part
-    if (ok && i > 0 && mbar_wait_warp(bar(B_ODONE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, tb.status, abort_flag)) {
+    if (ok && i > 0 && mbar_wait_warp(bar(B_SFREE + (i - 1) % NSB), ((i - 1) / NSB) & 1, tb.status, abort_flag)) {
       tc_fence_after();
       const bool write = r < tile.nrows;
       const int64_t qrow = (int64_t(j) * sh.rows + tile.nrow0 + r) * sh.Hq + h;

@@ -146,6 +146,11 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
 }
 
+// 32 consecutive 32-bit columns of this thread's TMEM lane, raw words.
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* r) {
+  tmem_st32(taddr, reinterpret_cast<const float*>(r));
+}
+
 // 16 consecutive 32-bit columns of this thread's TMEM lane (e.g. 32 bf16 packed in pairs).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
