@@ -11,6 +11,10 @@
 #define BA_FWD_BN 64    // keys per forward key block (work estimate only)
 #define BA_BWD_BM 64    // query rows per backward query tile
 #define BA_BWD_BN 128   // keys per backward key tile
+#define BA_BWD_CS 2     // key tiles per thread-block cluster of the dK/dV kernel:
+                        // the tiles of a cluster come from one chunk, meet the
+                        // same query tiles in the same order and share each
+                        // Q / dO tile through one multicast load
 
 // Device status word values (first word of the workspace).
 #define BA_DEV_OK 0u
@@ -45,7 +49,11 @@ struct BaKvSeg {
   int32_t diag;    // 1: the per-row causal limit cuts into the segment
 };
 
-// Backward: a run of <= BN packed main keys inside one chunk.
+// Backward: a run of <= BN packed main keys inside one chunk.  Key tiles come
+// in groups of BA_BWD_CS consecutive tiles of one chunk (consecutive in the
+// table, and in the launch order) that share one list of query ranges; a
+// group at the end of a chunk is filled up with empty tiles (nkeys = 0) that
+// take part in the group's loads but own no keys.
 struct BaKvTile {
   int32_t k0, nkeys, pos0;
   int32_t qr0, nqr;   // query-tile ranges that see this key tile, ring-replay order

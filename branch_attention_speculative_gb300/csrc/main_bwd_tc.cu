@@ -36,6 +36,14 @@
 // other's latencies), warp 8 loads with TMA (Q, dO and the tile's 16-byte row
 // records {lse*log2e, Delta, key limit}) into a 4-stage ring, warp 9 issues the
 // MMAs and owns TMEM.  All waits are bounded.
+// Clusters: BA_BWD_CS CTAs that own consecutive key tiles of one chunk (and
+// one kv head) form a thread-block cluster.  They meet the same query tiles in
+// the same order, so each stage of the Q / dO ring is loaded once for the
+// cluster: every CTA issues a share of the stage's boxes as multicast TMA loads
+// into all of them, and a stage is refilled only when every CTA's dV / dK
+// GEMMs have released it (their commits arrive on every CTA's empty barrier).
+// That divides the Q / dO traffic from L2 and DRAM by the cluster size and
+// keeps the cluster's sweeps in step.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -52,6 +60,8 @@ constexpr int NTHREADS = 320;  // 8 compute warps, 1 TMA warp, 1 MMA warp
 
 constexpr int NQS = 4;    // query-tile pipeline stages
 constexpr int NSB = 3;    // S^T buffers in TMEM
+constexpr int CS = BA_BWD_CS;
+constexpr uint16_t CMASK = uint16_t((1u << CS) - 1u);
 
 struct BwdSmem {
   static constexpr uint32_t KT = 128u * 128u;  // [128 keys][64 d] bf16 block
@@ -151,14 +161,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const BaShape& sh = a.sh;
   const BaTables& tb = a.tb;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int kvh = int(blockIdx.x % sh.Hkv);
-  const int oi = int(blockIdx.x / sh.Hkv);
-  if (oi >= tb.n_bkv) {
+  // blockIdx.x = (group * Hkv + kvh) * CS + rank in the cluster
+  const int crank = int(blockIdx.x % CS);
+  const int cid = int(blockIdx.x / CS);
+  const int kvh = cid % sh.Hkv;
+  const int gi = cid / sh.Hkv;
+  if ((gi + 1) * CS > tb.n_bkv) {  // the same for every CTA of the cluster
     if (tid == 0) ba_set_status(tb.status, BA_DEV_BOUNDS);
     return;
   }
-  if (*reinterpret_cast<volatile unsigned int*>(tb.status) != 0u) return;
-  const BaKvTile kt = tb.bkv[tb.border[oi]];
+  const BaKvTile kt = tb.bkv[tb.border[gi * CS + crank]];
   const int nstream = sh.steps * sh.G;
 
   if (tid == 0) {
@@ -166,7 +178,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(bar(B_KV), 1);
     for (int s = 0; s < NQS; ++s) {
       mbar_init(bar(B_QFULL + s), 1);
-      mbar_init(bar(B_QEMPTY + s), 1);
+      mbar_init(bar(B_QEMPTY + s), CS);  // one release per CTA of the cluster
     }
     for (int s = 0; s < NSB; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
@@ -184,6 +196,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // every CTA's barriers are initialised before any multicast reaches them
+  if constexpr (CS > 1) cluster_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem, tDP = tmem + 192, tDK = tmem + 256, tDV = tmem + 384;
   const bool any = kt.nqr > 0;
@@ -207,20 +221,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       QIter it;
       it.init(tb.bqr, kt.qr0, kt.nqr, nstream);
-      for (int i = 0; it.valid(); ++i, it.next()) {
+      int i = 0;
+      bool pok = true;
+      for (; it.valid(); ++i, it.next()) {
         const int st = i % NQS;
         const uint32_t ph = (i / NQS) & 1;
-        if (!mbar_wait(bar(B_QEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
+        if (!mbar_wait(bar(B_QEMPTY + st), ph ^ 1, tb.status, abort_flag)) { pok = false; break; }
         const BaQTile qt = tb.bq[it.ti];
         const int j = it.sx / sh.G, h = kvh * sh.G + it.sx % sh.G;
         const int qrow = int(int64_t(j) * sh.rows + qt.nrow0);
         const int srow = int((int64_t(j) * sh.Hq + h) * sh.rows + qt.nrow0);
         mbar_expect_tx(bar(B_QFULL + st), 4 * L::QT + L::META);
-        for (int cb = 0; cb < 2; ++cb) {
-          tma_load_3d(sbase + L::q + (st * 2 + cb) * L::QT, &tmq, bar(B_QFULL + st), cb * 64, h, qrow);
-          tma_load_3d(sbase + L::go + (st * 2 + cb) * L::QT, &tmdo, bar(B_QFULL + st), cb * 64, h, qrow);
+        // the stage's five boxes (Q, dO in two 64-column blocks each, the row
+        // records); CTA `crank` of the cluster loads every CS-th one for all
+#pragma unroll
+        for (int pc = 0; pc < 5; ++pc) {
+          if (pc % CS != crank) continue;
+          const uint32_t fb = bar(B_QFULL + st);
+          if (pc < 4) {
+            const int cb = pc & 1;
+            const bool isq = pc < 2;
+            const uint32_t dst = sbase + (isq ? L::q : L::go) + (st * 2 + cb) * L::QT;
+            if constexpr (CS > 1)
+              tma_load_3d_mc(dst, isq ? &tmq : &tmdo, fb, cb * 64, h, qrow, CMASK);
+            else
+              tma_load_3d(dst, isq ? &tmq : &tmdo, fb, cb * 64, h, qrow);
+          } else {
+            if constexpr (CS > 1)
+              tma_load_2d_mc(sbase + L::meta + st * L::META, &tmrec, fb, 0, srow, CMASK);
+            else
+              tma_load_2d(sbase + L::meta + st * L::META, &tmrec, fb, 0, srow);
+          }
         }
-        tma_load_2d(sbase + L::meta + st * L::META, &tmrec, bar(B_QFULL + st), 0, srow);
+      }
+      // the other CTAs' releases of the last stages land on this CTA's
+      // barriers: wait for them before the CTA may leave
+      if constexpr (CS > 1) {
+        for (int x = i > NQS ? i - NQS : 0; pok && x < i; ++x)
+          pok = mbar_wait(bar(B_QEMPTY + x % NQS), (x / NQS) & 1, tb.status, abort_flag);
       }
     }
   } else if (warp == 9) {
@@ -268,7 +306,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar(B_SEMPTY + i % NSB));
-        tc_commit(bar(B_QEMPTY + qs));
+        if constexpr (CS > 1)
+          tc_commit_mc(bar(B_QEMPTY + qs), CMASK);  // released in every CTA of the cluster
+        else
+          tc_commit(bar(B_QEMPTY + qs));
       }
       tc_commit(bar(B_DONE));
     }
@@ -377,6 +418,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if constexpr (CS > 1) {
+    // no CTA leaves while another may still write into its shared memory:
+    // after a failed wait give copies and commits already in flight time to
+    // land, then meet the rest of the cluster
+    if (*abort_flag) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < (1ll << 21)) {
+      }
+    }
+    cluster_sync();
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -441,6 +493,19 @@ cudaError_t ba_launch_main_bwd_kv_tc(const BaBwdArgs& a, cudaStream_t st) {
   if ((e = cudaFuncSetAttribute(main_bwd_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
       cudaSuccess)
     return e;
-  main_bwd_kv_tc_kernel<<<unsigned(grid), NTHREADS, smem, st>>>(a, mq, mdo, mk, mv, mrec);
+  if (grid % CS != 0) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, main_bwd_kv_tc_kernel, a, mq, mdo, mk, mv, mrec)) != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -262,44 +262,65 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
   make_qtiles(BA_BWD_BM, p->bq, &bfirst, &bcount);
   p->bkv.clear();
   p->bqr.clear();
+  std::vector<int32_t> gwork;  // per group of BA_BWD_CS key tiles
   for (int32_t gid : chunk_order) {
     const BaChunk& kch = p->chunks[gid];
-    for (int32_t k0 = 0; k0 < kch.len; k0 += BA_BWD_BN) {
-      BaKvTile kt{};
-      kt.k0 = kch.pk0 + k0;
-      kt.nkeys = std::min(BA_BWD_BN, kch.len - k0);
-      kt.pos0 = kch.nat0 + k0;
-      kt.chunk = gid;
-      kt.qr0 = int32_t(p->bqr.size());
-      kt.work = 0;
-      // The query chunks this key tile meets are those the ring replay brings
-      // to it (rank (r + s) mod C at step s): every later chunk of the
-      // sequence, unmasked, and its own chunk, cut by the causal limit.  They
-      // are listed unmasked chunks first, in descending chunk order — a prefix
-      // shared by every key tile of the sequence, so key tiles that run at the
-      // same time stream the same Q / dO tiles and share them in L2 — and the
-      // diagonal chunk last.  Only the summation order of dK / dV depends on it.
+    const int32_t ntiles = (kch.len + BA_BWD_BN - 1) / BA_BWD_BN;
+    for (int32_t g0 = 0; g0 < ntiles; g0 += BA_BWD_CS) {
+      // The query chunks a key tile meets are those the ring replay brings to
+      // it (rank (r + s) mod C at step s): every later chunk of the sequence,
+      // unmasked, and its own chunk, cut by the causal limit.  They are listed
+      // unmasked chunks first, in descending chunk order — a prefix shared by
+      // every key tile of the sequence — and the diagonal chunk last.  The
+      // tiles of a group share one list: on the diagonal chunk it starts at the
+      // first query tile that sees the group's first (lowest) key, so it holds
+      // every query tile any member sees; the per-row limits mask the rest.
+      // Only the summation order of dK / dV depends on the order.
+      const int32_t gpos0 = kch.nat0 + g0 * BA_BWD_BN;
+      const int32_t qr0 = int32_t(p->bqr.size());
+      int32_t work = 0;
       for (int qc = nch - 1; qc >= kch.c; --qc) {
         const int32_t qg = kch.seq * nch + qc;
         int32_t t0 = bfirst[qg], t1 = bfirst[qg] + bcount[qg];
         int diag = 0;
         if (qc == kch.c) {
-          while (t0 < t1 && p->bq[t0].lim_max < kt.pos0) ++t0;
+          while (t0 < t1 && p->bq[t0].lim_max < gpos0) ++t0;
           diag = 1;
         }
         if (t0 >= t1) continue;
         p->bqr.push_back(BaQRange{t0, t1, diag, 0});
-        kt.work += t1 - t0;
+        work += t1 - t0;
       }
-      kt.nqr = int32_t(p->bqr.size()) - kt.qr0;
-      // kept even when no query sees it: its dK / dV must still be written (as zeros)
-      p->bkv.push_back(kt);
+      const int32_t nqr = int32_t(p->bqr.size()) - qr0;
+      for (int32_t m = 0; m < BA_BWD_CS; ++m) {
+        const int32_t t = g0 + m;
+        BaKvTile kt{};
+        if (t < ntiles) {
+          kt.k0 = kch.pk0 + t * BA_BWD_BN;
+          kt.nkeys = std::min(BA_BWD_BN, kch.len - t * BA_BWD_BN);
+          kt.pos0 = kch.nat0 + t * BA_BWD_BN;
+        } else {  // filler: no keys; loads point at the chunk's first tile
+          kt.k0 = kch.pk0;
+          kt.nkeys = 0;
+          kt.pos0 = kch.nat0;
+        }
+        kt.chunk = gid;
+        kt.qr0 = qr0;
+        kt.nqr = nqr;
+        kt.work = work;
+        // kept even when no query sees it: its dK / dV must still be written (as zeros)
+        p->bkv.push_back(kt);
+      }
+      gwork.push_back(work);
     }
   }
-  p->border.resize(p->bkv.size());
-  for (size_t i = 0; i < p->bkv.size(); ++i) p->border[i] = int32_t(i);
-  std::stable_sort(p->border.begin(), p->border.end(),
-                   [&](int32_t x, int32_t y) { return p->bkv[x].work > p->bkv[y].work; });
+  // groups longest first; the members of a group stay consecutive
+  std::vector<int32_t> gorder(gwork.size());
+  for (size_t g = 0; g < gwork.size(); ++g) gorder[g] = int32_t(g);
+  std::stable_sort(gorder.begin(), gorder.end(), [&](int32_t x, int32_t y) { return gwork[x] > gwork[y]; });
+  p->border.clear();
+  for (int32_t g : gorder)
+    for (int32_t m = 0; m < BA_BWD_CS; ++m) p->border.push_back(g * BA_BWD_CS + m);
 
   // ---- Eq. 3 volume from the schedule
   std::vector<int64_t> shard(C, 0);
@@ -414,9 +435,17 @@ int ba_validate_plan(const ba_plan* p) {
   }
   for (const BaQTile& t : p->bq)
     if (!check_tile(t, BA_BWD_BM)) return bad();
-  for (const BaKvTile& k : p->bkv) {
-    if (k.k0 < 0 || k.nkeys < 1 || k.nkeys > BA_BWD_BN || int64_t(k.k0) + k.nkeys > T) return bad();
-    if (p->tok_perm[k.k0] != k.pos0 || p->tok_perm[k.k0 + k.nkeys - 1] != k.pos0 + k.nkeys - 1) return bad();
+  if (p->bkv.size() % BA_BWD_CS != 0) return bad();
+  for (size_t i = 0; i < p->bkv.size(); ++i) {
+    const BaKvTile& k = p->bkv[i];
+    const BaKvTile& lead = p->bkv[i - i % BA_BWD_CS];
+    // a group shares its chunk and its query ranges; only members after the
+    // first may be empty fillers, and a filler is followed only by fillers
+    if (k.chunk != lead.chunk || k.qr0 != lead.qr0 || k.nqr != lead.nqr) return bad();
+    if (i % BA_BWD_CS == 0 ? k.nkeys < 1 : (k.nkeys > 0 && p->bkv[i - 1].nkeys == 0)) return bad();
+    if (k.k0 < 0 || k.nkeys < 0 || k.nkeys > BA_BWD_BN || int64_t(k.k0) + std::max(k.nkeys, 1) > T) return bad();
+    if (p->tok_perm[k.k0] != k.pos0) return bad();
+    if (k.nkeys > 0 && p->tok_perm[k.k0 + k.nkeys - 1] != k.pos0 + k.nkeys - 1) return bad();
     if (k.qr0 < 0 || k.nqr < 0 || int64_t(k.qr0) + k.nqr > int64_t(p->bqr.size())) return bad();
     for (int i = 0; i < k.nqr; ++i) {
       const BaQRange& r = p->bqr[k.qr0 + i];
@@ -445,5 +474,10 @@ int ba_validate_plan(const ba_plan* p) {
     return true;
   };
   if (!is_perm(p->forder, p->fq.size()) || !is_perm(p->border, p->bkv.size())) return bad();
+  // the launch order keeps the members of a group together and in order
+  for (size_t i = 0; i < p->border.size(); ++i)
+    if (p->border[i] != p->border[i - i % BA_BWD_CS] + int32_t(i % BA_BWD_CS) ||
+        p->border[i - i % BA_BWD_CS] % BA_BWD_CS != 0)
+      return bad();
   return BA_OK;
 }
