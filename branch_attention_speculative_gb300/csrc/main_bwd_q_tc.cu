@@ -187,6 +187,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (elect_one()) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, KBN, false, false);  // S, dP
       constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);     // dQ (K as MN-major B)
+      // operand descriptors, built once: every MMA below adds a constant offset
+      const uint64_t dq0 = smem_desc_sw128(sbase + L::q, 16, 1024), dg0 = smem_desc_sw128(sbase + L::go, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sbase + L::k, 16, 1024), dv0 = smem_desc_sw128(sbase + L::v, 16, 1024);
+      const uint64_t dkm = smem_desc_sw128(sbase + L::k, L::TILE, 1024);
       auto issue_dp = [&](int i) -> bool {
         const int vs = i % NV;
         if (!mbar_wait(bar(B_VFULL + vs), (i / NV) & 1, tb.status, abort_flag)) return false;
@@ -195,8 +199,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
-          tc_mma(tDP, smem_desc_sw128(sbase + L::go + off, 16, 1024),
-                 smem_desc_sw128(sbase + L::v + vs * 2 * L::TILE + off, 16, 1024), id_s, kk > 0);
+          tc_mma(tDP, desc_add(dg0, off), desc_add(dv0, vs * 2 * L::TILE + off), id_s, kk > 0);
         }
         tc_commit(bar(B_VEMPTY + vs));
         return true;
@@ -209,8 +212,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
-          tc_mma(tS + sb * KBN, smem_desc_sw128(sbase + L::q + off, 16, 1024),
-                 smem_desc_sw128(sbase + L::k + ks * 2 * L::TILE + off, 16, 1024), id_s, kk > 0);
+          tc_mma(tS + sb * KBN, desc_add(dq0, off), desc_add(dk0, ks * 2 * L::TILE + off), id_s, kk > 0);
         }
         tc_commit(bar(B_SFULL + sb));  // also covers dP(i), issued before
         return true;
@@ -219,11 +221,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int ks = i % NK, sb = i & 1;
         if (!mbar_wait(bar(B_DSFULL + sb), (i >> 1) & 1, tb.status, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t kbase = sbase + L::k + ks * 2 * L::TILE;
+        const uint64_t dks = desc_add(dkm, ks * 2 * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < KBN / 16; ++kk)
-          tc_mma_tmem_a(tDQ, tS + sb * KBN + (kk >> 2) * 64 + (kk & 3) * 8,
-                        smem_desc_sw128(kbase + kk * 2048, L::TILE, 1024), id_q, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_tmem_a(tDQ, tS + sb * KBN + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(dks, kk * 2048), id_q,
+                        (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar(B_SFREE + sb));
         tc_commit(bar(B_KEMPTY + ks));
         return true;

@@ -268,6 +268,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);     // dV, dK
       int n = 0;
       for (int r = kt.qr0; r < kt.qr0 + kt.nqr; ++r) n += (tb.bqr[r].t1 - tb.bqr[r].t0) * nstream;
+      // operand descriptors, built once: every MMA below adds a constant offset
+      const uint64_t dk0 = smem_desc_sw128(sbase + L::k, 16, 1024), dv0 = smem_desc_sw128(sbase + L::v, 16, 1024);
+      const uint64_t dq0 = smem_desc_sw128(sbase + L::q, 16, 1024), dg0 = smem_desc_sw128(sbase + L::go, 16, 1024);
+      const uint64_t dqm = smem_desc_sw128(sbase + L::q, L::QT, 1024), dgm = smem_desc_sw128(sbase + L::go, L::QT, 1024);
       auto issue_sdp = [&](int i) -> bool {
         const int qs = i % NQS;
         const int sb = i % NSB;
@@ -275,14 +279,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(bar(B_SEMPTY + sb), ((i / NSB) & 1) ^ 1, tb.status, abort_flag)) return false;
         if (!mbar_wait(bar(B_DPEMPTY), (i & 1) ^ 1, tb.status, abort_flag)) return false;
         tc_fence_after();
+        const uint64_t dqs = desc_add(dq0, qs * 2 * L::QT), dgs = desc_add(dg0, qs * 2 * L::QT);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ok_ = (kk >> 2) * L::KT + (kk & 3) * 32;
           const uint32_t oq = (kk >> 2) * L::QT + (kk & 3) * 32;
-          tc_mma(tS + sb * 64, smem_desc_sw128(sbase + L::k + ok_, 16, 1024),
-                 smem_desc_sw128(sbase + L::q + qs * 2 * L::QT + oq, 16, 1024), id_s, kk > 0);
-          tc_mma(tDP, smem_desc_sw128(sbase + L::v + ok_, 16, 1024),
-                 smem_desc_sw128(sbase + L::go + qs * 2 * L::QT + oq, 16, 1024), id_s, kk > 0);
+          tc_mma(tS + sb * 64, desc_add(dk0, ok_), desc_add(dqs, oq), id_s, kk > 0);
+          tc_mma(tDP, desc_add(dv0, ok_), desc_add(dgs, oq), id_s, kk > 0);
         }
         tc_commit(bar(B_SFULL + sb));
         return true;
@@ -294,16 +297,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(bar(B_PFULL + i % NSB), (i / NSB) & 1, tb.status, abort_flag)) break;
         tc_fence_after();
         const int qs = i % NQS;
-        const uint32_t qb = sbase + L::q + qs * 2 * L::QT, gb = sbase + L::go + qs * 2 * L::QT;
+        const uint64_t dqs = desc_add(dqm, qs * 2 * L::QT), dgs = desc_add(dgm, qs * 2 * L::QT);
         const uint32_t pa = tS + (i % NSB) * 64;
 #pragma unroll
         for (int kk = 0; kk < QBM / 16; ++kk) {
           // queries 16 kk .. 16 kk + 15 sit in query half kk / 2 of the buffer
           const uint32_t col = (kk >> 1) * 32 + (kk & 1) * 8;
-          tc_mma_tmem_a(tDV, pa + col, smem_desc_sw128(gb + kk * 2048, L::QT, 1024), id_kv,
-                        (i > 0 || kk > 0) ? 1u : 0u);
-          tc_mma_tmem_a(tDK, pa + col + 16, smem_desc_sw128(qb + kk * 2048, L::QT, 1024), id_kv,
-                        (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_tmem_a(tDV, pa + col, desc_add(dgs, kk * 2048), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_tmem_a(tDK, pa + col + 16, desc_add(dqs, kk * 2048), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar(B_SEMPTY + i % NSB));
         if constexpr (CS > 1)

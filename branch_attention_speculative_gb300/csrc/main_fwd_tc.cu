@@ -183,17 +183,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (elect_one()) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, TBN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      // operand descriptors, built once: every MMA below adds a constant offset
+      const uint64_t dq0 = smem_desc_sw128(sbase + L::q, 16, 1024), dk0 = smem_desc_sw128(sbase + L::k, 16, 1024);
+      const uint64_t dvm = smem_desc_sw128(sbase + L::v, L::TILE, 1024);
       auto issue_pv = [&](int i) -> bool {
         const int pb = i % NSB, vs = i % NKV;
         if (!mbar_wait(bar(B_PFULL + pb), (i / NSB) & 1, tb.status, abort_flag)) return false;
         if (!mbar_wait(bar(B_VFULL + vs), (i / NKV) & 1, tb.status, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t vbase = sbase + L::v + vs * CB * L::TILE;
+        const uint64_t dvs = desc_add(dvm, vs * CB * L::TILE);
 #pragma unroll
-        for (int kk = 0; kk < TBN / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, L::TILE, 1024);
-          tc_mma_tmem_a(tO, tS + pb * TBN + kk * 8, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < TBN / 16; ++kk)
+          tc_mma_tmem_a(tO, tS + pb * TBN + kk * 8, desc_add(dvs, kk * 2048), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar(B_SFREE + pb));
         tc_commit(bar(B_VEMPTY + vs));
         return true;
@@ -207,12 +208,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(bar(B_KFULL + ks), (i / NKV) & 1, tb.status, abort_flag)) { ok = false; break; }
         if (!mbar_wait(bar(B_SFREE + sb), ((i / NSB) & 1) ^ 1, tb.status, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kbase = sbase + L::k + ks * CB * L::TILE;
+        const uint64_t dks = desc_add(dk0, ks * CB * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
-          tc_mma(tS + sb * TBN, smem_desc_sw128(sbase + L::q + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024),
-                 idesc_qk, kk > 0 ? 1u : 0u);
+          tc_mma(tS + sb * TBN, desc_add(dq0, off), desc_add(dks, off), idesc_qk, kk > 0 ? 1u : 0u);
         }
         tc_commit(bar(B_SFULL + sb));
         tc_commit(bar(B_KEMPTY + ks));

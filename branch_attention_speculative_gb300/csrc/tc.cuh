@@ -208,6 +208,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Descriptor of (base + byte_off) from the descriptor of base: only the start
+// address field (bits 0-13, address >> 4) changes, and CTA shared-memory
+// addresses stay below 256 KB, so the sum never carries out of the field.
+// Lets the MMA-issuing thread build each descriptor with one add.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t byte_off) { return d + (byte_off >> 4); }
+
 // Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, M x N, operand majors.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                      // D format: fp32
