@@ -326,6 +326,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // after a failed wait, give MMAs and copies already in flight time to land
+  // before TMEM is released
+  if (*abort_flag) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < (1ll << 21)) {
+    }
+  }
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

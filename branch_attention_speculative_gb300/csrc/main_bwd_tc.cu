@@ -415,21 +415,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // after a failed wait, give copies, MMAs and commits already in flight time
+  // to land before TMEM is released and the CTA leaves
+  if (*abort_flag) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < (1ll << 21)) {
+    }
+  }
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if constexpr (CS > 1) {
-    // no CTA leaves while another may still write into its shared memory:
-    // after a failed wait give copies and commits already in flight time to
-    // land, then meet the rest of the cluster
-    if (*abort_flag) {
-      const long long t0 = clock64();
-      while (clock64() - t0 < (1ll << 21)) {
-      }
-    }
-    cluster_sync();
-  }
+  // no CTA leaves while another may still write into its shared memory
+  if constexpr (CS > 1) cluster_sync();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;

@@ -19,9 +19,13 @@
 //              than 2^8 (the values of P stay below 256), and finally writes
 //              O_m = O / l and l_m.
 //   warp 4     TMA producer: Q once, then K and V blocks into three-stage rings.
-//   warp 5     MMA issuer (one thread): S = Q K^T into one of three TMEM S
-//              buffers, then O += P V for the previous block with P read from
-//              TMEM as the A operand; owns TMEM.
+//   warp 5     owns TMEM; one thread issues S = Q K^T into one of three TMEM
+//              S buffers.
+//   warp 6     one thread issues O += P V with P read from TMEM as the A
+//              operand.  Two issuing threads: an MMA instruction is accepted
+//              only as fast as the tensor cores take it, so a single thread
+//              that also waits on the softmax between groups lets the queue
+//              run dry; each thread's commits track its own GEMMs.
 // TMEM: S buffers at columns [0,128), [128,256), [256,384); O = [384, 384 + d).
 // An S buffer is busy from its QK^T GEMM until the PV GEMM of the same block
 // has read P out of it, so with three of them the next block's QK^T is always
@@ -40,7 +44,7 @@ namespace {
 
 constexpr int TBM = 128;  // query rows per tile
 constexpr int TBN = 128;  // keys per block
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 224;  // 4 softmax warps, 1 TMA warp, 2 MMA-issuing warps
 constexpr int NKV = 3;    // K / V ring stages
 constexpr int NSB = 3;    // S (and P) buffers in TMEM
 
@@ -178,8 +182,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tma_load_3d(sbase + L::v + (st * CB + cb) * L::TILE, &tmv, bar(B_VFULL + st), cb * 64, kvh, key);
       }
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 5 || warp == 6) {
+    // ------------------------------------------------------------ MMA issuers
     if (elect_one()) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, TBN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
@@ -203,22 +207,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       BlockIter it;
       it.init(tb.fseg, tile.seg0, tile.nseg);
       int i = 0;
-      for (; ok && it.valid(); ++i, it.next()) {
-        const int ks = i % NKV, sb = i % NSB;
-        if (!mbar_wait(bar(B_KFULL + ks), (i / NKV) & 1, tb.status, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(bar(B_SFREE + sb), ((i / NSB) & 1) ^ 1, tb.status, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t dks = desc_add(dk0, ks * CB * L::TILE);
+      if (warp == 5) {
+        for (; ok && it.valid(); ++i, it.next()) {
+          const int ks = i % NKV, sb = i % NSB;
+          if (!mbar_wait(bar(B_KFULL + ks), (i / NKV) & 1, tb.status, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar(B_SFREE + sb), ((i / NSB) & 1) ^ 1, tb.status, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t dks = desc_add(dk0, ks * CB * L::TILE);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
-          tc_mma(tS + sb * TBN, desc_add(dq0, off), desc_add(dks, off), idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
+            tc_mma(tS + sb * TBN, desc_add(dq0, off), desc_add(dks, off), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(B_SFULL + sb));
+          tc_commit(bar(B_KEMPTY + ks));
         }
-        tc_commit(bar(B_SFULL + sb));
-        tc_commit(bar(B_KEMPTY + ks));
-        if (i > 0 && !issue_pv(i - 1)) { ok = false; break; }
+      } else {
+        for (; it.valid(); ++i, it.next())
+          if (!issue_pv(i)) break;
       }
-      if (ok && i > 0) issue_pv(i - 1);
     }
   } else {
     // ------------------------------------------------------------ softmax (rows)
@@ -327,6 +334,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // after a failed wait, give MMAs and copies already in flight time to land
+  // before TMEM is released
+  if (*abort_flag) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < (1ll << 21)) {
+    }
+  }
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
