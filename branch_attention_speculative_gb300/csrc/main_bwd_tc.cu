@@ -20,13 +20,11 @@
 // dK and dV stay in TMEM for the whole CTA and are written once, in natural
 // order, at the end.  dQ is computed by the query-stationary kernel
 // (main_bwd_q_tc.cu), which needs no atomics.
-// TMEM columns: three S^T buffers [0,64) [64,128) [128,192), one dP^T buffer
-// [192,256), dK [256,384), dV [384,512).  An S^T buffer stays busy from its
-// S^T GEMM until the dV/dK GEMMs of the same pair have read P^T / dS^T out of
-// it; the dP^T buffer is free as soon as the threads have loaded it.  With
-// three S^T buffers the S^T/dP^T GEMMs of the next pair are always queued
-// behind the dV/dK GEMMs of the current one, and the threads' exp work on a
-// pair overlaps the tensor cores' work on its neighbours.
+// TMEM columns: S^T buffers [0,64) and [64,128), dP^T buffers [128,192) and
+// [192,256), dK [256,384), dV [384,512); pair i uses buffers i % 2.  An S^T
+// buffer stays busy from its S^T GEMM until the dV/dK GEMMs of the same pair
+// have read P^T / dS^T out of it; a dP^T buffer is free as soon as the threads
+// have loaded it.
 // Inside an S^T buffer the compute warp of query half h (queries 32h..32h+31)
 // reads fp32 columns [32h, 32h+32) and writes back, into the same columns,
 // P^T (bf16 pairs) at [32h, 32h+16) and dS^T at [32h+16, 32h+32); no warp
@@ -34,8 +32,14 @@
 // Warp roles: warps 0-7 compute (warp w: TMEM lane quarter w % 4 = key rows,
 // query columns 32 (w / 4) ..; two warps per SM sub-partition hide each
 // other's latencies), warp 8 loads with TMA (Q, dO and the tile's 16-byte row
-// records {lse*log2e, Delta, key limit}) into a 4-stage ring, warp 9 issues the
-// MMAs and owns TMEM.  All waits are bounded.
+// records {lse*log2e, Delta, key limit}) into a 4-stage ring, and three warps
+// each have one thread issue one kind of GEMM: warp 9 (which owns TMEM) S^T,
+// warp 11 dP^T, warp 10 dV and dK.  One tcgen05.mma costs the issuing thread
+// about as long as the tensor cores take to run an N=64 one, so a single
+// issuer, which also waits on the compute warps between groups, cannot keep
+// the queue full; three can.  Each thread's commits track its own GEMMs; the
+// S^T / dP^T pair of a tile signals its readiness with one commit from each
+// issuer on a two-arrival barrier.  All waits are bounded.
 // Clusters: BA_BWD_CS CTAs that own consecutive key tiles of one chunk (and
 // one kv head) form a thread-block cluster.  They meet the same query tiles in
 // the same order, so each stage of the Q / dO ring is loaded once for the
@@ -56,10 +60,10 @@ namespace {
 
 constexpr int KBN = 128;  // keys per CTA
 constexpr int QBM = 64;   // queries per tile
-constexpr int NTHREADS = 320;  // 8 compute warps, 1 TMA warp, 1 MMA warp
+constexpr int NTHREADS = 384;  // 8 compute warps, 1 TMA warp, 3 MMA-issuing warps
 
 constexpr int NQS = 4;    // query-tile pipeline stages
-constexpr int NSB = 3;    // S^T buffers in TMEM
+constexpr int NSB = 2;    // S^T and dP^T buffers in TMEM (each)
 constexpr int CS = BA_BWD_CS;
 constexpr uint16_t CMASK = uint16_t((1u << CS) - 1u);
 
@@ -81,12 +85,10 @@ enum {
   B_KV = 0,
   B_QFULL = 1,                 // [NQS]
   B_QEMPTY = B_QFULL + NQS,    // [NQS]
-  B_SFULL = B_QEMPTY + NQS,    // [NSB] S^T and dP^T of a pair are in TMEM
-  B_SEMPTY = B_SFULL + NSB,    // [NSB] dV/dK of the pair have read the buffer
-  B_DPEMPTY = B_SEMPTY + NSB,  // the threads have loaded dP^T
-  B_PFULL = B_DPEMPTY + 1,     // [NSB] P^T and dS^T are in TMEM (one barrier per
-                               // buffer: the threads can finish a pair before the
-                               // MMA warp has waited for the previous one)
+  B_SFULL = B_QEMPTY + NQS,    // [NSB] S^T and dP^T of a pair are in TMEM (2 commits)
+  B_SEMPTY = B_SFULL + NSB,    // [NSB] dV/dK of the pair have read its S^T buffer
+  B_DPEMPTY = B_SEMPTY + NSB,  // [NSB] the threads have loaded the dP^T buffer
+  B_PFULL = B_DPEMPTY + NSB,   // [NSB] P^T and dS^T are in TMEM
   B_DONE = B_PFULL + NSB,
   B_COUNT = B_DONE + 1
 };
@@ -181,11 +183,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_QEMPTY + s), CS);  // one release per CTA of the cluster
     }
     for (int s = 0; s < NSB; ++s) {
-      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_SFULL + s), 2);  // the S^T and the dP^T issuer
       mbar_init(bar(B_SEMPTY + s), 1);
+      mbar_init(bar(B_DPEMPTY + s), 8);
       mbar_init(bar(B_PFULL + s), 8);
     }
-    mbar_init(bar(B_DPEMPTY), 8);
     mbar_init(bar(B_DONE), 1);
     fence_mbar_init();
   }
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // every CTA's barriers are initialised before any multicast reaches them
   if constexpr (CS > 1) cluster_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tDP = tmem + 192, tDK = tmem + 256, tDV = tmem + 384;
+  const uint32_t tS = tmem, tDP = tmem + 128, tDK = tmem + 256, tDV = tmem + 384;
   const bool any = kt.nqr > 0;
 
   if (warp == 8) {
@@ -261,39 +263,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           pok = mbar_wait(bar(B_QEMPTY + x % NQS), (x / NQS) & 1, tb.status, abort_flag);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 11) {
+    // ------------------------------------------------------------ S^T (warp 9) / dP^T (warp 11) issuers
     if (elect_one() && any) {
-      constexpr uint32_t id_s = idesc_bf16_f32(128, QBM, false, false);   // S^T, dP^T
-      constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);     // dV, dK
+      constexpr uint32_t id_s = idesc_bf16_f32(128, QBM, false, false);
       int n = 0;
       for (int r = kt.qr0; r < kt.qr0 + kt.nqr; ++r) n += (tb.bqr[r].t1 - tb.bqr[r].t0) * nstream;
+      const bool is_s = warp == 9;
       // operand descriptors, built once: every MMA below adds a constant offset
-      const uint64_t dk0 = smem_desc_sw128(sbase + L::k, 16, 1024), dv0 = smem_desc_sw128(sbase + L::v, 16, 1024);
-      const uint64_t dq0 = smem_desc_sw128(sbase + L::q, 16, 1024), dg0 = smem_desc_sw128(sbase + L::go, 16, 1024);
-      const uint64_t dqm = smem_desc_sw128(sbase + L::q, L::QT, 1024), dgm = smem_desc_sw128(sbase + L::go, L::QT, 1024);
-      auto issue_sdp = [&](int i) -> bool {
-        const int qs = i % NQS;
-        const int sb = i % NSB;
-        if (!mbar_wait(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) return false;
-        if (!mbar_wait(bar(B_SEMPTY + sb), ((i / NSB) & 1) ^ 1, tb.status, abort_flag)) return false;
-        if (!mbar_wait(bar(B_DPEMPTY), (i & 1) ^ 1, tb.status, abort_flag)) return false;
-        tc_fence_after();
-        const uint64_t dqs = desc_add(dq0, qs * 2 * L::QT), dgs = desc_add(dg0, qs * 2 * L::QT);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ok_ = (kk >> 2) * L::KT + (kk & 3) * 32;
-          const uint32_t oq = (kk >> 2) * L::QT + (kk & 3) * 32;
-          tc_mma(tS + sb * 64, desc_add(dk0, ok_), desc_add(dqs, oq), id_s, kk > 0);
-          tc_mma(tDP, desc_add(dv0, ok_), desc_add(dgs, oq), id_s, kk > 0);
-        }
-        tc_commit(bar(B_SFULL + sb));
-        return true;
-      };
+      const uint64_t da = smem_desc_sw128(sbase + (is_s ? L::k : L::v), 16, 1024);
+      const uint64_t db = smem_desc_sw128(sbase + (is_s ? L::q : L::go), 16, 1024);
+      const uint32_t td = is_s ? tS : tDP;
+      const int free_bar = is_s ? B_SEMPTY : B_DPEMPTY;
       bool ok = mbar_wait(bar(B_KV), 0, tb.status, abort_flag);
-      if (ok && n > 0) ok = issue_sdp(0);
       for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n && !issue_sdp(i + 1)) break;
+        const int qs = i % NQS, sb = i % NSB;
+        if (!mbar_wait(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) break;
+        if (!mbar_wait(bar(free_bar + sb), ((i / NSB) & 1) ^ 1, tb.status, abort_flag)) break;
+        tc_fence_after();
+        const uint64_t dbs = desc_add(db, qs * 2 * L::QT);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma(td + sb * 64, desc_add(da, (kk >> 2) * L::KT + (kk & 3) * 32),
+                 desc_add(dbs, (kk >> 2) * L::QT + (kk & 3) * 32), id_s, kk > 0);
+        tc_commit(bar(B_SFULL + sb));
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ dV / dK issuer
+    if (elect_one() && any) {
+      constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
+      int n = 0;
+      for (int r = kt.qr0; r < kt.qr0 + kt.nqr; ++r) n += (tb.bqr[r].t1 - tb.bqr[r].t0) * nstream;
+      const uint64_t dqm = smem_desc_sw128(sbase + L::q, L::QT, 1024), dgm = smem_desc_sw128(sbase + L::go, L::QT, 1024);
+      for (int i = 0; i < n; ++i) {
+        // P^T / dS^T of the pair are in TMEM; its S^T / dP^T GEMMs (the other
+        // threads') had completed before the compute warps produced them
         if (!mbar_wait(bar(B_PFULL + i % NSB), (i / NSB) & 1, tb.status, abort_flag)) break;
         tc_fence_after();
         const int qs = i % NQS;
@@ -306,6 +311,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tc_mma_tmem_a(tDV, pa + col, desc_add(dgs, kk * 2048), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
           tc_mma_tmem_a(tDK, pa + col + 16, desc_add(dqs, kk * 2048), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
         }
+        // the pair's last readers of its S^T buffer and its Q / dO stage
         tc_commit(bar(B_SEMPTY + i % NSB));
         if constexpr (CS > 1)
           tc_commit_mc(bar(B_QEMPTY + qs), CMASK);  // released in every CTA of the cluster
@@ -314,7 +320,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       tc_commit(bar(B_DONE));
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ compute
     // warp w: TMEM lane quarter w % 4 (key rows 32 (w % 4) ..), query columns
     // 32 (w / 4) .. 32 (w / 4) + 31 of each 64-query tile
@@ -339,11 +345,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       float s[32], dp[32];
       tmem_ld32(tS + lane_off + sb * 64 + col0, s);
-      tmem_ld32(tDP + lane_off + col0, dp);
+      tmem_ld32(tDP + lane_off + sb * 64 + col0, dp);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DPEMPTY));  // the dP^T buffer is free again
+      if (lane == 0) mbar_arrive(bar(B_DPEMPTY + sb));  // the dP^T buffer is free again
       // row records {lse*log2e, Delta, limit, 0}; queries past the tile are masked
       const float* rec = reinterpret_cast<const float*>(gbase + L::meta + qs * L::META) + 4 * col0;
       const int nq = qt.nrows - col0;
