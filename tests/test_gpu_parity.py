@@ -132,6 +132,13 @@ SMALL = [
     W.small("causal", [136, 8, 256], heads_q=4, heads_kv=4, head_dim=64, cp=2, seed=5, name="causal_mha"),
     W.small("block", [64], heads_q=2, heads_kv=1, head_dim=64, cp=2, block=1, anchors_per_seq=1, seed=6,
             name="block_one_anchor"),
+    # chunks of several whole 128-key / 64- and 128-query tiles plus a ragged
+    # tail, at head_dim 128: every main key's dK/dV, including the unmasked
+    # key tiles away from the diagonal, is checked against the full oracle
+    W.small("ttt", [1280, 768], heads_q=8, heads_kv=2, head_dim=128, cp=2, depth=2, seed=7,
+            name="ttt_d128_tiles_c2"),
+    W.small("block", [1536, 512], heads_q=8, heads_kv=2, head_dim=128, cp=2, block=16, anchors_per_seq=40, seed=8,
+            name="block16_d128_tiles_c2"),
 ]
 
 
