@@ -10,25 +10,31 @@
 // because Eq. 2's merged result is the single softmax over their union).
 //
 // Per (query tile, key tile) pair, on the tensor cores:
-//   S^T  = K Q^T        M=128 keys, N=64 queries, K=d        -> TMEM (2 buffers)
-//   dP^T = V dO^T       same                                  -> TMEM (2 buffers)
+//   S^T  = K Q^T        M=128 keys, N=64 queries, K=d; K read from TMEM  -> TMEM S^T buffer
+//   dP^T = V dO^T       same, V a shared-memory operand                   -> TMEM dP^T buffer
 //   (threads)  P^T = exp2(S^T * scale*log2e - lse*log2e),  dS^T = P^T (dP^T - Delta)
-//              written back as bf16 into the S^T buffer they came from
+//              written as bf16 into the P/dS buffer
 //   dV  += P^T dO       M=128 keys, N=d, K=64 queries; P^T read from TMEM,
 //                       dO an MN-major shared operand
 //   dK  += dS^T Q       same, dS^T from TMEM
 // dK and dV stay in TMEM for the whole CTA and are written once, in natural
 // order, at the end.  dQ is computed by the query-stationary kernel
 // (main_bwd_q_tc.cu), which needs no atomics.
-// TMEM columns: S^T buffers [0,64) and [64,128), dP^T buffers [128,192) and
-// [192,256), dK [256,384), dV [384,512); pair i uses buffers i % 2.  An S^T
-// buffer stays busy from its S^T GEMM until the dV/dK GEMMs of the same pair
-// have read P^T / dS^T out of it; a dP^T buffer is free as soon as the threads
-// have loaded it.
-// Inside an S^T buffer the compute warp of query half h (queries 32h..32h+31)
-// reads fp32 columns [32h, 32h+32) and writes back, into the same columns,
-// P^T (bf16 pairs) at [32h, 32h+16) and dS^T at [32h+16, 32h+32); no warp
-// writes a column another warp still has to read.
+// Shared-memory bandwidth, not the tensor pipe, bounds this shape: an N=64
+// GEMM with both operands in shared memory reads 6 KB per 32-cycle MMA, more
+// than the 128 bytes per clock shared memory delivers.  The key tile is
+// stationary, so the threads copy K into TMEM once and the S^T GEMM reads only
+// its Q operand from shared memory.
+// TMEM columns: K (bf16 pairs) [0,64), S^T [64,128), dP^T [128,192), P/dS
+// [192,256), dK [256,384), dV [384,512).  The S^T and dP^T buffers are free
+// again as soon as the threads have loaded them, so the next pair's S^T and
+// dP^T GEMMs run while the threads work on this one.  The P/dS buffer is busy
+// from the threads' P^T store until the pair's dK GEMM has read it; the
+// threads compute the next pair's P^T in registers meanwhile.  The threads
+// store P^T first and signal it, so the dV GEMM runs while they compute dS^T;
+// the dK GEMM follows dS^T.  Inside the P/dS buffer the warp of query half h
+// (queries 32h..32h+31) writes P^T (bf16 pairs) at [32h, 32h+16) and dS^T at
+// [32h+16, 32h+32).
 // Warp roles: warps 0-7 compute (warp w: TMEM lane quarter w % 4 = key rows,
 // query columns 32 (w / 4) ..; two warps per SM sub-partition hide each
 // other's latencies), warp 8 loads with TMA (Q, dO and the tile's 16-byte row
@@ -37,9 +43,8 @@
 // warp 11 dP^T, warp 10 dV and dK.  One tcgen05.mma costs the issuing thread
 // about as long as the tensor cores take to run an N=64 one, so a single
 // issuer, which also waits on the compute warps between groups, cannot keep
-// the queue full; three can.  Each thread's commits track its own GEMMs; the
-// S^T / dP^T pair of a tile signals its readiness with one commit from each
-// issuer on a two-arrival barrier.  All waits are bounded.
+// the queue full; three can.  Each thread's commits track its own GEMMs.
+// All waits are bounded.
 // Clusters: BA_BWD_CS CTAs that own consecutive key tiles of one chunk (and
 // one kv head) form a thread-block cluster.  They meet the same query tiles in
 // the same order, so each stage of the Q / dO ring is loaded once for the
@@ -63,7 +68,6 @@ constexpr int QBM = 64;   // queries per tile
 constexpr int NTHREADS = 384;  // 8 compute warps, 1 TMA warp, 3 MMA-issuing warps
 
 constexpr int NQS = 4;    // query-tile pipeline stages
-constexpr int NSB = 2;    // S^T and dP^T buffers in TMEM (each)
 constexpr int CS = BA_BWD_CS;
 constexpr uint16_t CMASK = uint16_t((1u << CS) - 1u);
 
@@ -82,14 +86,18 @@ struct BwdSmem {
 };
 
 enum {
-  B_KV = 0,
-  B_QFULL = 1,                 // [NQS]
+  B_KV = 0,                    // K and V are in shared memory
+  B_KT = 1,                    // K is in TMEM (one arrival per compute warp)
+  B_QFULL = 2,                 // [NQS]
   B_QEMPTY = B_QFULL + NQS,    // [NQS]
-  B_SFULL = B_QEMPTY + NQS,    // [NSB] S^T and dP^T of a pair are in TMEM (2 commits)
-  B_SEMPTY = B_SFULL + NSB,    // [NSB] dV/dK of the pair have read its S^T buffer
-  B_DPEMPTY = B_SEMPTY + NSB,  // [NSB] the threads have loaded the dP^T buffer
-  B_PFULL = B_DPEMPTY + NSB,   // [NSB] P^T and dS^T are in TMEM
-  B_DONE = B_PFULL + NSB,
+  B_SFULL = B_QEMPTY + NQS,    // S^T of a pair is in TMEM
+  B_SEMPTY = B_SFULL + 1,      // the threads have loaded the S^T buffer
+  B_DPFULL = B_SEMPTY + 1,     // dP^T of a pair is in TMEM
+  B_DPEMPTY = B_DPFULL + 1,    // the threads have loaded the dP^T buffer
+  B_PFULL = B_DPEMPTY + 1,     // P^T is in the P/dS buffer
+  B_DSFULL = B_PFULL + 1,      // dS^T is in the P/dS buffer
+  B_PDSEMPTY = B_DSFULL + 1,   // dV/dK of the pair have read the P/dS buffer
+  B_DONE = B_PDSEMPTY + 1,
   B_COUNT = B_DONE + 1
 };
 static_assert(8 * B_COUNT + 16 <= 256, "barrier area");
@@ -178,16 +186,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(bar(B_KV), 1);
+    mbar_init(bar(B_KT), 8);
     for (int s = 0; s < NQS; ++s) {
       mbar_init(bar(B_QFULL + s), 1);
       mbar_init(bar(B_QEMPTY + s), CS);  // one release per CTA of the cluster
     }
-    for (int s = 0; s < NSB; ++s) {
-      mbar_init(bar(B_SFULL + s), 2);  // the S^T and the dP^T issuer
-      mbar_init(bar(B_SEMPTY + s), 1);
-      mbar_init(bar(B_DPEMPTY + s), 8);
-      mbar_init(bar(B_PFULL + s), 8);
-    }
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SEMPTY), 8);  // one arrival per compute warp
+    mbar_init(bar(B_DPFULL), 1);
+    mbar_init(bar(B_DPEMPTY), 8);
+    mbar_init(bar(B_PFULL), 8);
+    mbar_init(bar(B_DSFULL), 8);
+    mbar_init(bar(B_PDSEMPTY), 1);
     mbar_init(bar(B_DONE), 1);
     fence_mbar_init();
   }
@@ -201,7 +211,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // every CTA's barriers are initialised before any multicast reaches them
   if constexpr (CS > 1) cluster_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tDP = tmem + 128, tDK = tmem + 256, tDV = tmem + 384;
+  const uint32_t tK = tmem, tS = tmem + 64, tDP = tmem + 128, tPD = tmem + 192, tDK = tmem + 256, tDV = tmem + 384;
   const bool any = kt.nqr > 0;
 
   if (warp == 8) {
@@ -221,18 +231,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     if (lane == 0) {
+      // Q / dO rows and the record row of pair state `q`
+      auto coords = [&](const QIter& q, int& h, int& qrow, int& srow) {
+        const BaQTile qt = tb.bq[q.ti];
+        const int j = q.sx / sh.G;
+        h = kvh * sh.G + q.sx % sh.G;
+        qrow = int(int64_t(j) * sh.rows + qt.nrow0);
+        srow = int((int64_t(j) * sh.Hq + h) * sh.rows + qt.nrow0);
+      };
       QIter it;
       it.init(tb.bqr, kt.qr0, kt.nqr, nstream);
       int i = 0;
       bool pok = true;
-      for (; it.valid(); ++i, it.next()) {
+      int h = 0, qrow = 0, srow = 0;
+      if (it.valid()) coords(it, h, qrow, srow);
+      for (; it.valid(); ++i) {
         const int st = i % NQS;
         const uint32_t ph = (i / NQS) & 1;
         if (!mbar_wait(bar(B_QEMPTY + st), ph ^ 1, tb.status, abort_flag)) { pok = false; break; }
-        const BaQTile qt = tb.bq[it.ti];
-        const int j = it.sx / sh.G, h = kvh * sh.G + it.sx % sh.G;
-        const int qrow = int(int64_t(j) * sh.rows + qt.nrow0);
-        const int srow = int((int64_t(j) * sh.Hq + h) * sh.rows + qt.nrow0);
         mbar_expect_tx(bar(B_QFULL + st), 4 * L::QT + L::META);
         // the stage's five boxes (Q, dO in two 64-column blocks each, the row
         // records); CTA `crank` of the cluster loads every CS-th one for all
@@ -255,6 +271,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               tma_load_2d(sbase + L::meta + st * L::META, &tmrec, fb, 0, srow);
           }
         }
+        // the next pair's table entry is read while this stage's loads fly
+        it.next();
+        if (it.valid()) coords(it, h, qrow, srow);
       }
       // the other CTAs' releases of the last stages land on this CTA's
       // barriers: wait for them before the CTA may leave
@@ -271,22 +290,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int r = kt.qr0; r < kt.qr0 + kt.nqr; ++r) n += (tb.bqr[r].t1 - tb.bqr[r].t0) * nstream;
       const bool is_s = warp == 9;
       // operand descriptors, built once: every MMA below adds a constant offset
-      const uint64_t da = smem_desc_sw128(sbase + (is_s ? L::k : L::v), 16, 1024);
+      const uint64_t da = smem_desc_sw128(sbase + L::v, 16, 1024);  // V (the dP^T GEMM's A)
       const uint64_t db = smem_desc_sw128(sbase + (is_s ? L::q : L::go), 16, 1024);
       const uint32_t td = is_s ? tS : tDP;
-      const int free_bar = is_s ? B_SEMPTY : B_DPEMPTY;
-      bool ok = mbar_wait(bar(B_KV), 0, tb.status, abort_flag);
+      const int full_bar = is_s ? B_SFULL : B_DPFULL, free_bar = is_s ? B_SEMPTY : B_DPEMPTY;
+      // S^T reads K from TMEM once the threads have copied it there
+      bool ok = mbar_wait(bar(is_s ? B_KT : B_KV), 0, tb.status, abort_flag);
       for (int i = 0; ok && i < n; ++i) {
-        const int qs = i % NQS, sb = i % NSB;
+        const int qs = i % NQS;
         if (!mbar_wait(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) break;
-        if (!mbar_wait(bar(free_bar + sb), ((i / NSB) & 1) ^ 1, tb.status, abort_flag)) break;
+        // one buffer: pair i - 1's values have been loaded by the threads
+        if (!mbar_wait(bar(free_bar), (i & 1) ^ 1, tb.status, abort_flag)) break;
         tc_fence_after();
         const uint64_t dbs = desc_add(db, qs * 2 * L::QT);
+        if (is_s) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma(td + sb * 64, desc_add(da, (kk >> 2) * L::KT + (kk & 3) * 32),
-                 desc_add(dbs, (kk >> 2) * L::QT + (kk & 3) * 32), id_s, kk > 0);
-        tc_commit(bar(B_SFULL + sb));
+          for (int kk = 0; kk < D / 16; ++kk)  // a k16 step of K spans 8 TMEM columns
+            tc_mma_tmem_a(td, tK + kk * 8, desc_add(dbs, (kk >> 2) * L::QT + (kk & 3) * 32), id_s, kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma(td, desc_add(da, (kk >> 2) * L::KT + (kk & 3) * 32), desc_add(dbs, (kk >> 2) * L::QT + (kk & 3) * 32),
+                   id_s, kk > 0);
+        }
+        tc_commit(bar(full_bar));
       }
     }
   } else if (warp == 10) {
@@ -297,22 +324,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int r = kt.qr0; r < kt.qr0 + kt.nqr; ++r) n += (tb.bqr[r].t1 - tb.bqr[r].t0) * nstream;
       const uint64_t dqm = smem_desc_sw128(sbase + L::q, L::QT, 1024), dgm = smem_desc_sw128(sbase + L::go, L::QT, 1024);
       for (int i = 0; i < n; ++i) {
-        // P^T / dS^T of the pair are in TMEM; its S^T / dP^T GEMMs (the other
-        // threads') had completed before the compute warps produced them
-        if (!mbar_wait(bar(B_PFULL + i % NSB), (i / NSB) & 1, tb.status, abort_flag)) break;
-        tc_fence_after();
         const int qs = i % NQS;
-        const uint64_t dqs = desc_add(dqm, qs * 2 * L::QT), dgs = desc_add(dgm, qs * 2 * L::QT);
-        const uint32_t pa = tS + (i % NSB) * 64;
+        const uint32_t pa = tPD, ph = i & 1;
+        // dV += P^T dO as soon as P^T is in TMEM
+        if (!mbar_wait(bar(B_PFULL), ph, tb.status, abort_flag)) break;
+        tc_fence_after();
+        const uint64_t dgs = desc_add(dgm, qs * 2 * L::QT);
 #pragma unroll
-        for (int kk = 0; kk < QBM / 16; ++kk) {
-          // queries 16 kk .. 16 kk + 15 sit in query half kk / 2 of the buffer
-          const uint32_t col = (kk >> 1) * 32 + (kk & 1) * 8;
-          tc_mma_tmem_a(tDV, pa + col, desc_add(dgs, kk * 2048), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-          tc_mma_tmem_a(tDK, pa + col + 16, desc_add(dqs, kk * 2048), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        // the pair's last readers of its S^T buffer and its Q / dO stage
-        tc_commit(bar(B_SEMPTY + i % NSB));
+        for (int kk = 0; kk < QBM / 16; ++kk)  // queries 16 kk .. 16 kk + 15 sit in query half kk / 2
+          tc_mma_tmem_a(tDV, pa + (kk >> 1) * 32 + (kk & 1) * 8, desc_add(dgs, kk * 2048), id_kv,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q once the threads have written dS^T
+        if (!mbar_wait(bar(B_DSFULL), ph, tb.status, abort_flag)) break;
+        tc_fence_after();
+        const uint64_t dqs = desc_add(dqm, qs * 2 * L::QT);
+#pragma unroll
+        for (int kk = 0; kk < QBM / 16; ++kk)
+          tc_mma_tmem_a(tDK, pa + (kk >> 1) * 32 + (kk & 1) * 8 + 16, desc_add(dqs, kk * 2048), id_kv,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+        // the pair's last readers of its P/dS buffer and its Q / dO stage
+        tc_commit(bar(B_PDSEMPTY));
         if constexpr (CS > 1)
           tc_commit_mc(bar(B_QEMPTY + qs), CMASK);  // released in every CTA of the cluster
         else
@@ -330,61 +361,100 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const bool kok = row < kt.nkeys;
     const int kpos = kt.pos0 + row;
+    // K into TMEM as the S^T GEMM's A operand: this thread's key row, d block
+    // `half` (128 bytes, 16-byte chunks at chunk ^ (row % 8) in the 128-byte
+    // swizzled tile) -> columns 32 half .. 32 half + 31, two d values each
+    if (any) {
+      if (!mbar_wait_warp(bar(B_KV), 0, tb.status, abort_flag)) {
+        // fall through: the issuers see the abort flag and skip their GEMMs
+      } else {
+        const unsigned char* krow = gbase + L::k + half * L::KT + row * 128;
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 v = *reinterpret_cast<const uint4*>(krow + ((j ^ (row & 7)) * 16));
+          w[4 * j] = v.x;
+          w[4 * j + 1] = v.y;
+          w[4 * j + 2] = v.z;
+          w[4 * j + 3] = v.w;
+        }
+        tmem_st32u(tK + lane_off + half * 32, w);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_KT));
+      }
+    }
     QIter it;
     it.init(tb.bqr, kt.qr0, kt.nqr, nstream);
     bool ok = true;
     int i = 0;
     for (; it.valid(); ++i, it.next()) {
-      const int qs = i % NQS, sb = i % NSB;
-      const uint32_t ph = (i / NSB) & 1;
-      const BaQTile qt = tb.bq[it.ti];
+      const int qs = i % NQS;
+      const uint32_t pd = tPD + lane_off + col0;  // this warp's columns of the P/dS buffer
+      const int nrows = tb.bq[it.ti].nrows;
       const bool diag = it.cur.diag != 0;
       // q_full: the row records of this tile are in shared memory
       if (!mbar_wait_warp(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) { ok = false; break; }
-      if (!mbar_wait_warp(bar(B_SFULL + sb), ph, tb.status, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(B_SFULL), i & 1, tb.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      float s[32], dp[32];
-      tmem_ld32(tS + lane_off + sb * 64 + col0, s);
-      tmem_ld32(tDP + lane_off + sb * 64 + col0, dp);
+      float p[32];
+      tmem_ld32(tS + lane_off + col0, p);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DPEMPTY + sb));  // the dP^T buffer is free again
+      if (lane == 0) mbar_arrive(bar(B_SEMPTY));  // the next pair's S^T GEMM may start
       // row records {lse*log2e, Delta, limit, 0}; queries past the tile are masked
-      const float* rec = reinterpret_cast<const float*>(gbase + L::meta + qs * L::META) + 4 * col0;
-      const int nq = qt.nrows - col0;
+      const uint32_t rec = sbase + L::meta + qs * L::META + 16 * col0;
+      const int nq = nrows - col0;
+      float delta[32];
       if (!diag && kok && nq >= 32) {
         // full tile (the common case): no mask, one 8-byte load per column
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float2 r = *reinterpret_cast<const float2*>(rec + 4 * c);
-          const float p = ex2_approx(fmaf(s[c], sh.scale_log2, -r.x));
-          s[c] = p;
-          dp[c] = p * (dp[c] - r.y);
+          const float2 r = lds_f2(rec + 16 * c);
+          p[c] = ex2_approx(fmaf(p[c], sh.scale_log2, -r.x));
+          delta[c] = r.y;
         }
       } else {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float4 r = *reinterpret_cast<const float4*>(rec + 4 * c);
+          const float4 r = lds_f4(rec + 16 * c);
           const bool v = kok && c < nq && (!diag || kpos <= __float_as_int(r.z));
-          const float p = ex2_approx(fmaf(s[c], sh.scale_log2, -r.x));
-          s[c] = v ? p : 0.f;
-          dp[c] = s[c] * (dp[c] - r.y);
+          const float e = ex2_approx(fmaf(p[c], sh.scale_log2, -r.x));
+          p[c] = v ? e : 0.f;
+          delta[c] = r.y;
         }
       }
-      // P^T and dS^T back into this warp's own columns of the S^T buffer
-      uint32_t pw[16], dw[16];
+      uint32_t w[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        pw[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
-        dw[e] = pack_bf16(dp[2 * e], dp[2 * e + 1]);
-      }
-      tmem_st16(tS + lane_off + sb * 64 + col0, pw);
-      tmem_st16(tS + lane_off + sb * 64 + col0 + 16, dw);
+      for (int e = 0; e < 16; ++e) w[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
+      // P^T into the P/dS buffer once pair i - 1's dV / dK GEMMs have read it
+      if (!mbar_wait_warp(bar(B_PDSEMPTY), (i & 1) ^ 1, tb.status, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      tmem_st16(pd, w);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL + sb));
+      if (lane == 0) mbar_arrive(bar(B_PFULL));
+      // dS^T = P^T (dP^T - Delta)
+      if (!mbar_wait_warp(bar(B_DPFULL), i & 1, tb.status, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      float dp[32];
+      tmem_ld32(tDP + lane_off + col0, dp);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DPEMPTY));  // the next pair's dP^T GEMM may start
+#pragma unroll
+      for (int c = 0; c < 32; ++c) dp[c] = p[c] * (dp[c] - delta[c]);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e] = pack_bf16(dp[2 * e], dp[2 * e + 1]);
+      tmem_st16(pd + 16, w);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DSFULL));
     }
     // epilogue: dK (scaled) and dV of this key tile, natural order; each warp
     // writes d-columns 64 (w / 4) .. 64 (w / 4) + 63 of its 32 key rows
