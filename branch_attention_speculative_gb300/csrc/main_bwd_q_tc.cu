@@ -280,24 +280,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DPEMPTY));
-      if (climit >= KBN) {  // full block (the common case): no mask
+      // dS = P (dP - Delta) in 32-key groups, each packed (keys 2c and 2c + 1
+      // of this half in column c) and stored into the first 32 of this warp's
+      // 64 columns of the S buffer while the next group is computed
 #pragma unroll
-        for (int e = 0; e < 64; ++e) s[e] = ex2_approx(fmaf(s[e], sh.scale_log2, -l2)) * (dp[e] - delta);
-      } else {
+      for (int g = 0; g < 2; ++g) {
+        if (climit >= KBN) {  // full block (the common case): no mask
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const int c = half * 64 + e;
-          const float p = ex2_approx(fmaf(s[e], sh.scale_log2, -l2));
-          s[e] = (c < climit ? p : 0.f) * (dp[e] - delta);
+          for (int e = 32 * g; e < 32 * g + 32; ++e)
+            s[e] = ex2_approx(fmaf(s[e], sh.scale_log2, -l2)) * (dp[e] - delta);
+        } else {
+#pragma unroll
+          for (int e = 32 * g; e < 32 * g + 32; ++e) {
+            const int c = half * 64 + e;
+            const float p = ex2_approx(fmaf(s[e], sh.scale_log2, -l2));
+            s[e] = (c < climit ? p : 0.f) * (dp[e] - delta);
+          }
         }
-      }
-      // dS (bf16, keys 2c and 2c + 1 of this half in column c) back into the
-      // first 32 of this warp's 64 columns of the S buffer
-      {
-        uint32_t w[32];
+        uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) w[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
-        tmem_st32u(tS + lane_off + sb * KBN + half * 64, w);
+        for (int e = 0; e < 16; ++e) w[e] = pack_bf16(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
+        tmem_st16(tS + lane_off + sb * KBN + half * 64 + g * 16, w);
       }
       tmem_wait_st();
       tc_fence_before();
