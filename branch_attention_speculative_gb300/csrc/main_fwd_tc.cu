@@ -98,6 +98,19 @@ struct BlockIter {
   }
 };
 
+// One row's 128 scores of a block out of TMEM (four 32-column loads, one
+// wait), with keys at or past `climit` set to -inf when the block is masked.
+__device__ __forceinline__ void load_scores(float (&s)[TBN], uint32_t taddr, bool masked, int climit) {
+#pragma unroll
+  for (int c = 0; c < TBN / 32; ++c) tmem_ld32(taddr + c * 32, s + c * 32);
+  tmem_wait_ld();
+  if (masked) {
+#pragma unroll
+    for (int c = 0; c < TBN; ++c)
+      if (c >= climit) s[c] = -INFINITY;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
     main_fwd_tc_kernel(const BaFwdArgs a, const __grid_constant__ CUtensorMap tmq,
@@ -243,82 +256,96 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!mbar_wait_warp(bar(B_SFULL + sb), ph, tb.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
       float s[TBN];
-      // S in two halves: the second half's TMEM load runs while the first
-      // half is masked and reduced
-      tmem_ld32(tS + lane_off + sb * TBN, s);
-      tmem_ld32(tS + lane_off + sb * TBN + 32, s + 32);
-      tmem_wait_ld();
-      tmem_ld32(tS + lane_off + sb * TBN + 64, s + 64);
-      tmem_ld32(tS + lane_off + sb * TBN + 96, s + 96);
-      // mask: ragged end of the segment, causal limit on the diagonal chunk
       const int nvalid = it.cur.nkeys - it.kb;
       const bool masked = it.cur.diag || nvalid < TBN;
       const int climit = it.cur.diag ? min(nvalid, lim - (it.cur.pos0 + it.kb) + 1) : nvalid;
-      // row max as 8 independent chains (a single chain is 128 dependent steps)
-      float mxp[8];
-      if (masked) {
+      // S out of TMEM; mask: ragged end of the segment, causal limit on the
+      // diagonal chunk
+      load_scores(s, tS + lane_off + sb * TBN, masked, climit);
+      // Once every row of the warp has a reference max, the exponentials are
+      // taken against it without looking for the block max first: the block's
+      // row sum bounds each of its P values, so a sum within 2^8 shows that no
+      // row max grew by more than 2^8 and the result is exactly the one the
+      // max-first path gives.  Otherwise (a row's first keys, or a rare grow)
+      // the scores are reloaded and the block is done max-first.
+      bool fast = __all_sync(0xffffffffu, m_used != -INFINITY);
+      if (fast) {
+        float rsp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < TBN / 2; ++c)
-          if (c >= climit) s[c] = -INFINITY;
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mxp[k] = s[k];
-#pragma unroll
-      for (int c = 8; c < TBN / 2; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
-      tmem_wait_ld();
-      if (masked) {
-#pragma unroll
-        for (int c = TBN / 2; c < TBN; ++c)
-          if (c >= climit) s[c] = -INFINITY;
-      }
-#pragma unroll
-      for (int c = TBN / 2; c < TBN; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) mxp[k] = fmaxf(mxp[k], mxp[k + 4]);
-      const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
-      const float m_blk = mx * sh.scale_log2;
-      const bool grow = m_blk > m_used + 8.f;
-      const float m_next = grow ? m_blk : m_used;
-      const float base = m_next == -INFINITY ? 0.f : m_next;
-      // rescale O (warp-uniform TMEM access) when any row's max grew; PV of
-      // the previous block must have landed first
-      if (i >= 1 && __any_sync(0xffffffffu, grow)) {
-        const int pb = (i - 1) % NSB;
-        if (!mbar_wait_warp(bar(B_SFREE + pb), ((i - 1) / NSB) & 1, tb.status, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const float cfac = grow ? ex2_approx(m_used - base) : 1.f;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tmem_ld32(tO + lane_off + c * 32, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= cfac;
-          tmem_st32(tO + lane_off + c * 32, o);
-        }
-        tmem_wait_st();
-        l *= cfac;
-      } else if (grow) {
-        l *= ex2_approx(m_used - base);  // i == 0: O not written yet
-      }
-      m_used = m_next;
-      // P = exp2(S - base) in 32-key groups, each packed (keys 2c and 2c + 1
-      // in column c) and stored into this row's lane of the S buffer while the
-      // next group's exponentials run; only this thread reads or writes the lane
-      float rsp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int g = 0; g < TBN / 32; ++g) {
-#pragma unroll
-        for (int c = 32 * g; c < 32 * g + 32; ++c) {
-          s[c] = ex2_approx(fmaf(s[c], sh.scale_log2, -base));
+        for (int c = 0; c < TBN; ++c) {
+          s[c] = ex2_approx(fmaf(s[c], sh.scale_log2, -m_used));
           rsp[c & 7] += s[c];
         }
-        uint32_t w[16];
+        const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
+        if (__any_sync(0xffffffffu, rs > 256.f)) {
+          fast = false;
+          load_scores(s, tS + lane_off + sb * TBN, masked, climit);
+        } else {
+          l += rs;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = pack_bf16(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
-        tmem_st16(tS + lane_off + sb * TBN + g * 16, w);
+          for (int g = 0; g < TBN / 32; ++g) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = pack_bf16(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
+            tmem_st16(tS + lane_off + sb * TBN + g * 16, w);
+          }
+        }
       }
-      l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
+      if (!fast) {
+        // row max as 8 independent chains (a single chain is 128 dependent steps)
+        float mxp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mxp[k] = s[k];
+#pragma unroll
+        for (int c = 8; c < TBN; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mxp[k] = fmaxf(mxp[k], mxp[k + 4]);
+        const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
+        const float m_blk = mx * sh.scale_log2;
+        const bool grow = m_blk > m_used + 8.f;
+        const float m_next = grow ? m_blk : m_used;
+        const float base = m_next == -INFINITY ? 0.f : m_next;
+        // rescale O (warp-uniform TMEM access) when any row's max grew; PV of
+        // the previous block must have landed first
+        if (i >= 1 && __any_sync(0xffffffffu, grow)) {
+          const int pb = (i - 1) % NSB;
+          if (!mbar_wait_warp(bar(B_SFREE + pb), ((i - 1) / NSB) & 1, tb.status, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const float cfac = grow ? ex2_approx(m_used - base) : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tO + lane_off + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= cfac;
+            tmem_st32(tO + lane_off + c * 32, o);
+          }
+          tmem_wait_st();
+          l *= cfac;
+        } else if (grow) {
+          l *= ex2_approx(m_used - base);  // i == 0: O not written yet
+        }
+        m_used = m_next;
+        // P = exp2(S - base) in 32-key groups, each packed (keys 2c and 2c + 1
+        // in column c) and stored into this row's lane of the S buffer while
+        // the next group's exponentials run; only this thread reads or writes
+        // the lane
+        float rsp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int g = 0; g < TBN / 32; ++g) {
+#pragma unroll
+          for (int c = 32 * g; c < 32 * g + 32; ++c) {
+            s[c] = ex2_approx(fmaf(s[c], sh.scale_log2, -base));
+            rsp[c & 7] += s[c];
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = pack_bf16(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
+          tmem_st16(tS + lane_off + sb * TBN + g * 16, w);
+        }
+        l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
