@@ -240,8 +240,8 @@ def kernel_bytes(wl, info, name):
         return R * (2 * d * 4 + 2 * 4) + R * (d * 2 + 4)
     if name == "bwd_prep":  # read o, dO, lse; write the row record and zero the dQ row
         return R * (2 * d * 2 + 4) + R * (16 + d * 4)
-    if name == "branch_fwd":
-        return R * d * 2 + 2 * nbk * d * 2 + R * (d * 4 + 4)
+    if name == "branch_fwd":  # read q, k_b, v_b and the main partial (O_m fp32, l_m); write o (bf16) and lse
+        return R * d * 2 + 2 * nbk * d * 2 + R * (d * 4 + 4) + R * (d * 2 + 4)
     if name == "branch_bwd":
         return R * (2 * d * 2 + 2 * 4 + d * 4) + 2 * nbk * d * 2 + R * d * 2 + 2 * nbk * d * 2
     return None

@@ -245,14 +245,19 @@ int ba_forward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, c
   a.vb = v_b;
   a.om = reinterpret_cast<float*>(ws_at(workspace, w.om));
   a.lm = reinterpret_cast<float*>(ws_at(workspace, w.lm));
-  a.ob = reinterpret_cast<float*>(ws_at(workspace, w.ob));
-  a.lb = reinterpret_cast<float*>(ws_at(workspace, w.lb));
+  a.ob = nullptr;  // the branch kernel merges its rows as it computes them
+  a.lb = nullptr;
   a.o = o;
   a.lse = lse;
   BA_TRY(timed(p, K_MAIN_FWD, st,
                [&] { return use_mma_fwd() ? ba_launch_main_fwd(a, st) : ba_launch_main_fwd_tc(a, st); }));
-  if (has_b) BA_TRY(timed(p, K_BRANCH_FWD, st, [&] { return ba_launch_branch_fwd(a, st); }));
-  BA_TRY(timed(p, K_MERGE, st, [&] { return ba_launch_merge_plan(a, st); }));
+  // with branches, the branch kernel merges each row with the main part (Eq.
+  // 2) and writes o and lse; without, the main partial passes through the
+  // merge pass
+  if (has_b && p->shape.nbk > 0 && p->shape.units > 0)
+    BA_TRY(timed(p, K_BRANCH_FWD, st, [&] { return ba_launch_branch_fwd(a, st); }));
+  else
+    BA_TRY(timed(p, K_MERGE, st, [&] { return ba_launch_merge_plan(a, st); }));
   return BA_OK;
 }
 

@@ -14,6 +14,10 @@
 // products are warp-shuffle reductions.  The work is tiny next to the main
 // part and bound by HBM traffic of q, dO and the outputs.
 //
+// The forward also finishes the output: each row's branch part is merged with
+// the main part by Eq. 2 as soon as it is computed, so neither O_b nor a
+// separate merge pass over the rows touches HBM.
+//
 // The backward also finishes dQ: the main part arrives in the fp32
 // accumulator, the branch part is added here and the sum is written as bf16
 // in natural order (the finalize step, fused).
@@ -126,11 +130,37 @@ __global__ void __launch_bounds__(128) branch_fwd_kernel(BaFwdArgs a) {
         for (int e = 0; e < E; ++e) acc[e] = acc[e] * c + p * vs[i * D + lane * E + e];
         m = mn;
       }
-      const float inv = 1.f / l;
-      float* orow = a.ob + qrow * D + lane * E;
+      // Eq. 2 with the main part of the same row (its O_m and natural-log
+      // l_m are in the workspace): l = log(e^l_m + e^l_b) shifted by the
+      // larger of the two, O = e^(l_m - l) O_m + e^(l_b - l) O_b over the
+      // printed denominator; an empty part contributes nothing, whatever its
+      // O holds.  Written as the bf16 output row and the merged lse.
+      const float lb = (m + log2f(l)) * BA_LN2;
+      const float lm = a.lm[qrow];
+      const float top = fmaxf(lm, lb);
+      float res[E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) orow[e] = acc[e] * inv;
-      if (lane == 0) a.lb[qrow] = (m + log2f(l)) * BA_LN2;
+      for (int e = 0; e < E; ++e) res[e] = 0.f;
+      float lout = -INFINITY;
+      if (top != -INFINITY) {
+        lout = top + logf(expf(lm - top) + expf(lb - top));
+        const float wm = expf(lm - lout), wb = expf(lb - lout);
+        const float inv = 1.0f / (wm + wb);
+        if (wm > 0.f) {
+          const float* orow = a.om + qrow * D + lane * E;
+#pragma unroll
+          for (int e = 0; e < E; ++e) res[e] = wm * orow[e];
+        }
+        if (wb > 0.f) {
+          const float ib = wb / l;
+#pragma unroll
+          for (int e = 0; e < E; ++e) res[e] += ib * acc[e];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) res[e] *= inv;
+      }
+      store_row_bf16<D>(static_cast<__nv_bfloat16*>(a.o) + qrow * D, lane, res);
+      if (lane == 0) a.lse[qrow] = lout;
     }
   }
 }

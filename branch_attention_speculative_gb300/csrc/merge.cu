@@ -69,11 +69,11 @@ cudaError_t ba_launch_merge_rows(int64_t rows, int d, const float* om, const flo
   return cudaGetLastError();
 }
 
-// The plan's merge: every (step, row, head) of the query space; the CAUSAL
-// family has no branch part, so its main partial passes through.
+// The plan's merge pass over every (step, row, head) of the query space, used
+// when the plan has no branch keys (the CAUSAL family): the main partial
+// passes through (O_b absent, l_b = -inf).  With branch keys the branch
+// kernel merges each row itself.
 cudaError_t ba_launch_merge_plan(const BaFwdArgs& a, cudaStream_t st) {
   const int64_t rows = int64_t(a.sh.steps) * a.sh.rows * a.sh.Hq;
-  const bool has_b = a.sh.family != BA_FAMILY_CAUSAL;
-  return ba_launch_merge_rows(rows, a.sh.d, a.om, a.lm, has_b ? a.ob : nullptr, has_b ? a.lb : nullptr, a.o,
-                              a.lse, st);
+  return ba_launch_merge_rows(rows, a.sh.d, a.om, a.lm, nullptr, nullptr, a.o, a.lse, st);
 }

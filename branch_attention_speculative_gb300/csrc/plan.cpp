@@ -353,15 +353,15 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
   const size_t qrows = size_t(sh.steps) * size_t(rows) * size_t(sh.Hq);
   const size_t dd = size_t(sh.d);
   // The kernels read the caller's natural-layout tensors directly, so the
-  // workspace holds only partials: forward O_m, l_m (and O_b, l_b with
-  // branches), backward row records and the fp32 dQ accumulator.  The two
-  // regions overlap.
+  // workspace holds only partials: forward O_m, l_m (the branch kernel merges
+  // its part into the output row by row), backward row records and the fp32
+  // dQ accumulator.  The two regions overlap.
   const size_t scratch = off;
   size_t f = scratch;
   w.om = f; f = align256(f + qrows * dd * 4);
   w.lm = f; f = align256(f + qrows * 4);
-  w.ob = f; f = align256(f + (fam == BA_FAMILY_CAUSAL ? 0 : qrows * dd * 4));
-  w.lb = f; f = align256(f + (fam == BA_FAMILY_CAUSAL ? 0 : qrows * 4));
+  w.ob = f;  // no branch partials in the workspace
+  w.lb = f;
   size_t b = scratch;
   w.rowrec = b; b = align256(b + qrows * 16);
   w.dqacc = b; b = align256(b + qrows * dd * 4);

@@ -51,7 +51,7 @@ def test_noalloc_forward_matches_forward_twice(api, wl):
 
 
 def test_noalloc_rejects_plans_beyond_the_static_scratch(api):
-    wl = W.config(2)  # about 10 GB of workspace
+    wl = W.config(2)  # about 5 GB of workspace
     plan = api.Plan.from_workload(wl)
     assert plan.workspace_bytes > 64 << 20
     q = torch.empty(plan.q_shape(), dtype=torch.bfloat16, device="cuda")
