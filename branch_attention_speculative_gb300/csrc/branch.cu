@@ -63,6 +63,20 @@ __device__ __forceinline__ void load_row(const __nv_bfloat16* p, int lane, float
 }
 
 template <int D>
+__device__ __forceinline__ void load_row_f32(const float* p, int lane, float* x) {
+  constexpr int E = D / 32;
+  if constexpr (E == 4) {
+    const float4 v = reinterpret_cast<const float4*>(p)[lane];
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+    const float2 v = reinterpret_cast<const float2*>(p)[lane];
+    x[0] = v.x; x[1] = v.y;
+  }
+}
+
+constexpr int NKR = 8;  // branch keys per unit whose gradients a warp keeps in registers
+
+template <int D>
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* p, int lane, const float* x) {
   constexpr int E = D / 32;
   if constexpr (E == 4) {
@@ -75,15 +89,42 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* p, int lane, const
   }
 }
 
+// One unit's branch keys of one kv head into shared memory as fp32: row i of
+// ks / vs is key slot branch_slot(u, i).  16-byte loads of 8 values.
 template <int D>
 __device__ void stage_keys(const BaShape& sh, const __nv_bfloat16* kb, const __nv_bfloat16* vb, int64_t u, int kvh,
                            float* ks, float* vs) {
-  const int n = sh.nbk * D;
-  for (int e = threadIdx.x; e < n; e += blockDim.x) {
-    const int i = e / D, c = e % D;
-    const int64_t off = (branch_slot(sh, u, i) * sh.Hkv + kvh) * D + c;
-    ks[e] = __bfloat162float(kb[off]);
-    vs[e] = __bfloat162float(vb[off]);
+  constexpr int CH = D / 8;  // 16-byte chunks per key row
+  const int n = sh.nbk * CH;
+  for (int e = threadIdx.x; e < 2 * n; e += blockDim.x) {
+    const int m = e >= n ? 1 : 0;  // 0: K, 1: V
+    const int ee = e - m * n;
+    const int i = ee / CH, c = ee % CH;
+    const int64_t off = (branch_slot(sh, u, i) * sh.Hkv + kvh) * D + c * 8;
+    const uint4 v = *reinterpret_cast<const uint4*>((m ? vb : kb) + off);
+    const float2 a = unpack_bf16(v.x), b = unpack_bf16(v.y), c2 = unpack_bf16(v.z), d2 = unpack_bf16(v.w);
+    float4* dst = reinterpret_cast<float4*>((m ? vs : ks) + i * D + c * 8);
+    dst[0] = make_float4(a.x, a.y, b.x, b.y);
+    dst[1] = make_float4(c2.x, c2.y, d2.x, d2.y);
+  }
+}
+
+// dK_b / dV_b of one unit and kv head from shared memory (fp32) to their bf16
+// key slots.  16-byte stores of 8 values.
+template <int D>
+__device__ void store_key_grads(const BaShape& sh, __nv_bfloat16* dkb, __nv_bfloat16* dvb, int64_t u, int kvh,
+                                const float* dks, const float* dvs) {
+  constexpr int CH = D / 8;
+  const int n = sh.nbk * CH;
+  for (int e = threadIdx.x; e < 2 * n; e += blockDim.x) {
+    const int m = e >= n ? 1 : 0;
+    const int ee = e - m * n;
+    const int i = ee / CH, c = ee % CH;
+    const int64_t off = (branch_slot(sh, u, i) * sh.Hkv + kvh) * D + c * 8;
+    const float4* src = reinterpret_cast<const float4*>((m ? dvs : dks) + i * D + c * 8);
+    const float4 x = src[0], y = src[1];
+    *reinterpret_cast<uint4*>((m ? dvb : dkb) + off) =
+        make_uint4(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w), pack_bf16(y.x, y.y), pack_bf16(y.z, y.w));
   }
 }
 
@@ -193,6 +234,15 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
       for (int e = threadIdx.x; e < sh.nbk * D; e += blockDim.x) { dks[e] = 0.f; dvs[e] = 0.f; }
     }
     __syncthreads();
+    // Up to NKR keys (TTT up to depth 8): each warp keeps its rows' dK_b /
+    // dV_b contributions in registers and adds them to shared memory once per
+    // unit.  More keys (block branches): per-row shared-memory atomics.
+    const bool in_regs = sh.nbk <= NKR;
+    float dka[NKR][E], dva[NKR][E];
+#pragma unroll
+    for (int i = 0; i < NKR; ++i)
+#pragma unroll
+      for (int e = 0; e < E; ++e) dka[i][e] = dva[i][e] = 0.f;
     for (int idx = warp; idx < nq; idx += nwarps) {
       const int qi = idx / sh.G, g = idx % sh.G;
       int64_t j, r;
@@ -201,40 +251,70 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
       float q[E], go[E], gq[E];
       load_row<D>(qg + qrow * D, lane, q);
       load_row<D>(dog + qrow * D, lane, go);
-#pragma unroll
-      for (int e = 0; e < E; ++e) gq[e] = a.dqacc[qrow * D + lane * E + e];
+      load_row_f32<D>(a.dqacc + qrow * D, lane, gq);
       const int64_t srow = (j * sh.Hq + kvh * sh.G + g) * sh.rows + r;  // stream-major
       const float4 rec = a.rowrec[srow];
       const float l2 = rec.x;
       const float delta = rec.y;
       const int nk = keys_of_query(sh, qi);
-      for (int i = 0; i < nk; ++i) {
-        float dot = 0.f, dpv = 0.f;
+      if (in_regs) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          dot += q[e] * ks[i * D + lane * E + e];
-          dpv += go[e] * vs[i * D + lane * E + e];
+        for (int i = 0; i < NKR; ++i) {
+          if (i < nk) {
+            float dot = 0.f, dpv = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              dot += q[e] * ks[i * D + lane * E + e];
+              dpv += go[e] * vs[i * D + lane * E + e];
+            }
+            const float s2 = warp_sum(dot) * sh.scale_log2;
+            const float dp = warp_sum(dpv);
+            const float p = exp2f(s2 - l2);
+            const float ds = p * (dp - delta);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              gq[e] += sh.scale * ds * ks[i * D + lane * E + e];
+              dka[i][e] += sh.scale * ds * q[e];
+              dva[i][e] += p * go[e];
+            }
+          }
         }
-        const float s2 = warp_sum(dot) * sh.scale_log2;
-        const float dp = warp_sum(dpv);
-        const float p = exp2f(s2 - l2);
-        const float ds = p * (dp - delta);
+      } else {
+        for (int i = 0; i < nk; ++i) {
+          float dot = 0.f, dpv = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          gq[e] += sh.scale * ds * ks[i * D + lane * E + e];
-          atomicAdd(&dks[i * D + lane * E + e], sh.scale * ds * q[e]);
-          atomicAdd(&dvs[i * D + lane * E + e], p * go[e]);
+          for (int e = 0; e < E; ++e) {
+            dot += q[e] * ks[i * D + lane * E + e];
+            dpv += go[e] * vs[i * D + lane * E + e];
+          }
+          const float s2 = warp_sum(dot) * sh.scale_log2;
+          const float dp = warp_sum(dpv);
+          const float p = exp2f(s2 - l2);
+          const float ds = p * (dp - delta);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            gq[e] += sh.scale * ds * ks[i * D + lane * E + e];
+            atomicAdd(&dks[i * D + lane * E + e], sh.scale * ds * q[e]);
+            atomicAdd(&dvs[i * D + lane * E + e], p * go[e]);
+          }
         }
       }
       store_row_bf16<D>(dq + qrow * D, lane, gq);
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < sh.nbk * D; e += blockDim.x) {
-      const int i = e / D, c = e % D;
-      const int64_t off = (branch_slot(sh, u, i) * sh.Hkv + kvh) * D + c;
-      dkb[off] = __float2bfloat16_rn(dks[e]);
-      dvb[off] = __float2bfloat16_rn(dvs[e]);
+    if (in_regs) {
+#pragma unroll
+      for (int i = 0; i < NKR; ++i) {
+        if (i < sh.nbk) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            atomicAdd(&dks[i * D + lane * E + e], dka[i][e]);
+            atomicAdd(&dvs[i * D + lane * E + e], dva[i][e]);
+          }
+        }
+      }
     }
+    __syncthreads();
+    store_key_grads<D>(sh, dkb, dvb, u, kvh, dks, dvs);
   }
 }
 
