@@ -245,8 +245,6 @@ int ba_forward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, c
   a.vb = v_b;
   a.om = reinterpret_cast<float*>(ws_at(workspace, w.om));
   a.lm = reinterpret_cast<float*>(ws_at(workspace, w.lm));
-  a.ob = nullptr;  // the branch kernel merges its rows as it computes them
-  a.lb = nullptr;
   a.o = o;
   a.lse = lse;
   BA_TRY(timed(p, K_MAIN_FWD, st,

@@ -12,7 +12,7 @@ struct BaFwdArgs {
   BaShape sh;
   BaTables tb;
   const void *q, *km, *vm, *kb, *vb;  // inputs (bf16)
-  float *om, *lm, *ob, *lb;           // main and branch partials (fp32, workspace)
+  float *om, *lm;                     // main partials (fp32, workspace)
   void* o;                            // output (bf16)
   float* lse;                         // lse (fp32)
 };

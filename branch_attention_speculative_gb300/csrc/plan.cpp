@@ -360,8 +360,6 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
   size_t f = scratch;
   w.om = f; f = align256(f + qrows * dd * 4);
   w.lm = f; f = align256(f + qrows * 4);
-  w.ob = f;  // no branch partials in the workspace
-  w.lb = f;
   size_t b = scratch;
   w.rowrec = b; b = align256(b + qrows * 16);
   w.dqacc = b; b = align256(b + qrows * dd * 4);

@@ -15,7 +15,7 @@ struct BaWorkspaceLayout {
   size_t tables;                  // start of the uploaded table image
   size_t table_bytes;             // size of the table image
   size_t t_row_lim, t_nat_lim, t_tok_perm, t_anc_perm, t_fq, t_fseg, t_forder, t_bq, t_bkv, t_bqr, t_border;
-  size_t om, lm, ob, lb;          // forward partials (fp32, natural order)
+  size_t om, lm;                  // forward main partials (fp32, natural order)
   size_t rowrec, dqacc;           // backward scratch: row records (16 B), dQ (fp32), natural order
   size_t total;
 };
