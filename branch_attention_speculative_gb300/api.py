@@ -21,7 +21,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libba.so")
 
 FAMILY_CODES = {"ttt": 0, "block": 1, "causal": 2}
-TABLES = {"token_perm": 0, "anchor_perm": 1, "row_limit": 2, "token_rank": 3}
+TABLES = {"token_perm": 0, "anchor_perm": 1, "row_limit": 2, "token_rank": 3,
+          "fwd_qtiles": 4, "fwd_segs": 5, "bwd_qtiles": 6, "bwd_kvtiles": 7, "bwd_qranges": 8}
 ROLES = {"query": 0, "main_kv": 1, "branch_kv": 2}
 
 STATUS = {

@@ -6,6 +6,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <type_traits>
 
 #include "kernels.h"
 #include "plan.h"
@@ -199,20 +200,39 @@ int ba_plan_get_info(ba_plan_t p, ba_plan_info* info) {
   return BA_OK;
 }
 
+// record widths promised by ba.h for the schedule tables
+static_assert(sizeof(BaQTile) == 10 * sizeof(int32_t), "BA_TABLE_*_QTILES record");
+static_assert(sizeof(BaKvSeg) == 4 * sizeof(int32_t), "BA_TABLE_FWD_SEGS record");
+static_assert(sizeof(BaKvTile) == 8 * sizeof(int32_t), "BA_TABLE_BWD_KVTILES record");
+static_assert(sizeof(BaQRange) == 4 * sizeof(int32_t), "BA_TABLE_BWD_QRANGES record");
+
 int ba_plan_get_table(ba_plan_t p, int32_t which, int32_t* out, int64_t capacity, int64_t* count) {
   if (!p) return BA_ERR_INVALID_ARG;
-  const std::vector<int32_t>* v = nullptr;
+  // every schedule record is a run of int32 fields, copied out as they are
+  const void* src = nullptr;
+  int64_t n = 0;
+  auto pick = [&](const auto& v) {
+    using T = typename std::decay_t<decltype(v)>::value_type;
+    static_assert(sizeof(T) % sizeof(int32_t) == 0, "int32 records");
+    src = v.data();
+    n = int64_t(v.size()) * int64_t(sizeof(T) / sizeof(int32_t));
+  };
   switch (which) {
-    case BA_TABLE_TOKEN_PERM: v = &p->tok_perm; break;
-    case BA_TABLE_ANCHOR_PERM: v = &p->anc_perm; break;
-    case BA_TABLE_ROW_LIMIT: v = &p->row_lim; break;
-    case BA_TABLE_TOKEN_RANK: v = &p->tok_rank; break;
+    case BA_TABLE_TOKEN_PERM: pick(p->tok_perm); break;
+    case BA_TABLE_ANCHOR_PERM: pick(p->anc_perm); break;
+    case BA_TABLE_ROW_LIMIT: pick(p->row_lim); break;
+    case BA_TABLE_TOKEN_RANK: pick(p->tok_rank); break;
+    case BA_TABLE_FWD_QTILES: pick(p->fq); break;
+    case BA_TABLE_FWD_SEGS: pick(p->fseg); break;
+    case BA_TABLE_BWD_QTILES: pick(p->bq); break;
+    case BA_TABLE_BWD_KVTILES: pick(p->bkv); break;
+    case BA_TABLE_BWD_QRANGES: pick(p->bqr); break;
     default: return BA_ERR_INVALID_ARG;
   }
-  if (count) *count = int64_t(v->size());
+  if (count) *count = n;
   if (!out) return BA_OK;
-  if (capacity < int64_t(v->size())) return BA_ERR_INVALID_ARG;
-  if (!v->empty()) std::memcpy(out, v->data(), v->size() * sizeof(int32_t));
+  if (capacity < n) return BA_ERR_INVALID_ARG;
+  if (n > 0) std::memcpy(out, src, size_t(n) * sizeof(int32_t));
   return BA_OK;
 }
 

@@ -109,7 +109,23 @@ typedef enum {
   BA_TABLE_TOKEN_PERM = 0,   /* int32 [T]: packed token -> natural token         */
   BA_TABLE_ANCHOR_PERM = 1,  /* int32 [NA]: packed anchor -> natural anchor index */
   BA_TABLE_ROW_LIMIT = 2,    /* int32 [rows]: packed row -> last visible main pos */
-  BA_TABLE_TOKEN_RANK = 3    /* int32 [T]: natural token -> owning virtual rank   */
+  BA_TABLE_TOKEN_RANK = 3,   /* int32 [T]: natural token -> owning virtual rank   */
+  /* The main-attention schedule, as the kernels read it (int32 records):     */
+  BA_TABLE_FWD_QTILES = 4,   /* [n][10] forward query tiles: {row0, nrows, seg0,
+                                nseg, lim_min, lim_max, work, chunk, nrow0, 0};
+                                rows row0.. are packed rows (ROW_LIMIT index),
+                                nrow0.. the same rows in natural order          */
+  BA_TABLE_FWD_SEGS = 5,     /* [n][4] key segments of the forward tiles, ring
+                                order: {k0, nkeys, pos0, diag}; keys pos0 ..
+                                pos0 + nkeys - 1 (natural), cut by each row's
+                                limit when diag = 1                             */
+  BA_TABLE_BWD_QTILES = 6,   /* [n][10] backward query tiles, fields as FWD_QTILES */
+  BA_TABLE_BWD_KVTILES = 7,  /* [n][8] backward key tiles: {k0, nkeys, pos0, qr0,
+                                nqr, work, chunk, 0}; nkeys = 0 for the fillers
+                                that complete a cluster                         */
+  BA_TABLE_BWD_QRANGES = 8   /* [n][4] query-tile ranges of the key tiles, ring-
+                                replay order: {t0, t1, diag, 0} (BWD_QTILES
+                                indices t0 .. t1 - 1)                           */
 } ba_table;
 
 /* Build a plan: zigzag chunk map (2C chunks per sequence, rank r holding

@@ -142,3 +142,84 @@ def test_null_and_misaligned_pointers_rejected_before_launch(api):
     rc = lib.ba_forward(p._h, *([ctypes.c_void_p(0x1000)] * 7), None, 0, None)
     assert rc == -6
     assert lib.ba_lse_merge(4, 96, None, None, None, None, None, None, None) == -1
+
+
+# ---------------------------------------------------------------- the main-attention schedule
+#
+# The kernels see the main part only through the planner's tile tables.  These
+# checks rebuild, from those tables alone, which (query row, main key) pairs
+# the forward and the backward visit, and compare the result with the
+# oracle's main-key mask: every visible pair exactly once, nothing else.
+
+
+def _schedule_cases():
+    return [W.config(1),
+            W.small("ttt", [200, 56, 320], heads_q=4, heads_kv=2, head_dim=64, cp=2, depth=3, seed=1),
+            W.small("ttt", [1280, 768], heads_q=8, heads_kv=2, head_dim=128, cp=2, depth=2, seed=7),
+            W.small("ttt", [16, 32, 48], cp=4, depth=2),
+            W.small("block", [1536, 512], heads_q=8, heads_kv=2, head_dim=128, cp=2, block=16, anchors_per_seq=40,
+                    seed=8),
+            W.small("block", [96, 32, 160], heads_q=4, heads_kv=2, head_dim=64, cp=4, block=3, anchors_per_seq=7,
+                    seed=4),
+            W.small("causal", [136, 8, 256], heads_q=4, heads_kv=4, head_dim=64, cp=2, seed=5)]
+
+
+def _stream_rows(wl):
+    return wl.num_anchors * wl.block if wl.family == "block" else wl.tokens
+
+
+def _expected_cover(wl):
+    n = _stream_rows(wl)
+    return oracle.keysets.main_mask(wl, np.arange(n), np.arange(wl.tokens)).astype(np.int32)
+
+
+def _tile_rows(tile, row_limit):
+    row0, nrows, nrow0 = int(tile[0]), int(tile[1]), int(tile[8])
+    lim = row_limit[row0:row0 + nrows]
+    assert tile[4] == lim.min() and tile[5] == lim.max()
+    return nrow0 + np.arange(nrows), lim
+
+
+@pytest.mark.parametrize("wl", _schedule_cases(), ids=lambda w: w.name)
+def test_forward_schedule_covers_each_visible_pair_once(api, wl):
+    p = api.Plan.from_workload(wl)
+    lim = p.table("row_limit")
+    fq = p.table("fwd_qtiles").reshape(-1, 10)
+    fs = p.table("fwd_segs").reshape(-1, 4)
+    cover = np.zeros((_stream_rows(wl), wl.tokens), dtype=np.int32)
+    for tile in fq:
+        rows, rl = _tile_rows(tile, lim)
+        assert 0 < len(rows) <= 128
+        for k0, nkeys, pos0, diag in fs[tile[2]:tile[2] + tile[3]]:
+            keys = pos0 + np.arange(nkeys)
+            vis = keys[None, :] <= rl[:, None]
+            if diag:
+                assert vis.any()  # fully masked (tile, segment) pairs are dropped
+            else:
+                assert vis.all()  # an unmasked segment is below every row limit
+            cover[rows[:, None], keys[None, :]] += vis
+    assert np.array_equal(cover, _expected_cover(wl))
+
+
+@pytest.mark.parametrize("wl", _schedule_cases(), ids=lambda w: w.name)
+def test_backward_schedule_covers_each_visible_pair_once(api, wl):
+    p = api.Plan.from_workload(wl)
+    lim = p.table("row_limit")
+    bq = p.table("bwd_qtiles").reshape(-1, 10)
+    bkv = p.table("bwd_kvtiles").reshape(-1, 8)
+    br = p.table("bwd_qranges").reshape(-1, 4)
+    cover = np.zeros((_stream_rows(wl), wl.tokens), dtype=np.int32)
+    for k0, nkeys, pos0, qr0, nqr in bkv[:, :5]:
+        assert 0 <= nkeys <= 128
+        if nkeys == 0:  # a filler that completes a cluster owns no keys
+            continue
+        keys = pos0 + np.arange(nkeys)
+        for t0, t1, diag, _ in br[qr0:qr0 + nqr]:
+            for t in range(t0, t1):
+                rows, rl = _tile_rows(bq[t], lim)
+                assert 0 < len(rows) <= 64
+                vis = keys[None, :] <= rl[:, None]
+                if not diag:
+                    assert vis.all()
+                cover[rows[:, None], keys[None, :]] += vis
+    assert np.array_equal(cover, _expected_cover(wl))
