@@ -35,9 +35,10 @@ cudaError_t ba_launch_zigzag_gather(const void* src, void* dst, const int32_t* p
 // tcgen05 / TMEM / TMA kernel (the default) and the mma.sync kernel it replaces.
 cudaError_t ba_launch_main_fwd_tc(const BaFwdArgs& a, cudaStream_t st);
 cudaError_t ba_launch_main_fwd(const BaFwdArgs& a, cudaStream_t st);
-// K3: rank-local branch attention -> O_b, l_b.
+// K3 + K4: rank-local branch attention, each row merged with O_m, l_m by
+// Eq. 2 as it is computed -> o, lse.
 cudaError_t ba_launch_branch_fwd(const BaFwdArgs& a, cudaStream_t st);
-// K4: Eq. 2 merge of the partials -> o, lse.
+// K4 alone for plans without branch keys: O_m, l_m pass through -> o, lse.
 cudaError_t ba_launch_merge_plan(const BaFwdArgs& a, cudaStream_t st);
 // K4 on caller buffers.
 cudaError_t ba_launch_merge_rows(int64_t rows, int d, const float* om, const float* lm, const float* ob,
