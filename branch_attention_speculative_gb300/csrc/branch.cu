@@ -330,10 +330,10 @@ cudaError_t ba_launch_branch_fwd(const BaFwdArgs& a, cudaStream_t st) {
   if (total == 0 || a.sh.nbk == 0) return cudaSuccess;
   const size_t smem = size_t(2) * a.sh.nbk * a.sh.d * sizeof(float);
   if (a.sh.d == 128) {
-    cudaFuncSetAttribute(branch_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (cudaError_t e = set_dynamic_smem(branch_fwd_kernel<128>, smem); e != cudaSuccess) return e;
     branch_fwd_kernel<128><<<unsigned(grid_for(total)), 128, smem, st>>>(a);
   } else {
-    cudaFuncSetAttribute(branch_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (cudaError_t e = set_dynamic_smem(branch_fwd_kernel<64>, smem); e != cudaSuccess) return e;
     branch_fwd_kernel<64><<<unsigned(grid_for(total)), 128, smem, st>>>(a);
   }
   return cudaGetLastError();
@@ -344,10 +344,10 @@ cudaError_t ba_launch_branch_bwd(const BaBwdArgs& a, cudaStream_t st) {
   if (total == 0) return cudaSuccess;
   const size_t smem = size_t(4) * a.sh.nbk * a.sh.d * sizeof(float);
   if (a.sh.d == 128) {
-    cudaFuncSetAttribute(branch_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (cudaError_t e = set_dynamic_smem(branch_bwd_kernel<128>, smem); e != cudaSuccess) return e;
     branch_bwd_kernel<128><<<unsigned(grid_for(total)), 128, smem, st>>>(a);
   } else {
-    cudaFuncSetAttribute(branch_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (cudaError_t e = set_dynamic_smem(branch_bwd_kernel<64>, smem); e != cudaSuccess) return e;
     branch_bwd_kernel<64><<<unsigned(grid_for(total)), 128, smem, st>>>(a);
   }
   return cudaGetLastError();

@@ -31,6 +31,12 @@ struct BaBwdArgs {
 // K1: dst[o][i] = src[o][perm[i]] (inverse = 0) or dst[o][perm[i]] = src[o][i].
 cudaError_t ba_launch_zigzag_gather(const void* src, void* dst, const int32_t* perm, int64_t outer,
                                     int64_t units, int64_t unit_bytes, int inverse, cudaStream_t st);
+// Allows a kernel `bytes` of dynamic shared memory (host side, before a launch).
+template <class Kernel>
+inline cudaError_t set_dynamic_smem(Kernel* kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+}
+
 // K2: causal main attention over each query tile's key segments -> O_m, l_m.
 // tcgen05 / TMEM / TMA kernel (the default) and the mma.sync kernel it replaces.
 cudaError_t ba_launch_main_fwd_tc(const BaFwdArgs& a, cudaStream_t st);

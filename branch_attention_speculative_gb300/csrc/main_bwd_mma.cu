@@ -305,11 +305,11 @@ cudaError_t ba_launch_main_bwd(const BaBwdArgs& a, cudaStream_t st) {
   if (grid == 0) return cudaSuccess;
   if (a.sh.d == 128) {
     const int smem = int(BwdSmem<128>::bytes);
-    cudaFuncSetAttribute(main_bwd_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaError_t e = set_dynamic_smem(main_bwd_mma_kernel<128>, size_t(smem)); e != cudaSuccess) return e;
     main_bwd_mma_kernel<128><<<unsigned(grid), NT, smem, st>>>(a);
   } else {
     const int smem = int(BwdSmem<64>::bytes);
-    cudaFuncSetAttribute(main_bwd_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaError_t e = set_dynamic_smem(main_bwd_mma_kernel<64>, size_t(smem)); e != cudaSuccess) return e;
     main_bwd_mma_kernel<64><<<unsigned(grid), NT, smem, st>>>(a);
   }
   return cudaGetLastError();

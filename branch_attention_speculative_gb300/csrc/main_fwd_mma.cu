@@ -237,11 +237,11 @@ cudaError_t ba_launch_main_fwd(const BaFwdArgs& a, cudaStream_t st) {
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (a.sh.d == 128) {
     const int smem = (FBM + 4 * FBN) * (128 + 8) * 2;
-    cudaFuncSetAttribute(main_fwd_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaError_t e = set_dynamic_smem(main_fwd_mma_kernel<128>, size_t(smem)); e != cudaSuccess) return e;
     main_fwd_mma_kernel<128><<<unsigned(grid), 256, smem, st>>>(a);
   } else {
     const int smem = (FBM + 4 * FBN) * (64 + 8) * 2;
-    cudaFuncSetAttribute(main_fwd_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaError_t e = set_dynamic_smem(main_fwd_mma_kernel<64>, size_t(smem)); e != cudaSuccess) return e;
     main_fwd_mma_kernel<64><<<unsigned(grid), 256, smem, st>>>(a);
   }
   return cudaGetLastError();
