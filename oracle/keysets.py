@@ -8,7 +8,7 @@ from every position; DFlash generates a whole block in one pass; every branch
 attends the causal prefix and its own branch-local KV); rainbus page,
 prerequisites on the three draft families.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 * TTT: the step-j query (j = 1..D) anchored at main position p attends main
   keys [seq_start, p] (inclusive) and branch keys (p, i) for 1 <= i <= j.
   Stored 0-based: row (jj, p) attends branch keys (ii, p), ii <= jj.
