@@ -180,12 +180,8 @@ def _tile_rows(tile, row_limit):
     return nrow0 + np.arange(nrows), lim
 
 
-@pytest.mark.parametrize("wl", _schedule_cases(), ids=lambda w: w.name)
-def test_forward_schedule_covers_each_visible_pair_once(api, wl):
-    p = api.Plan.from_workload(wl)
-    lim = p.table("row_limit")
-    fq = p.table("fwd_qtiles").reshape(-1, 10)
-    fs = p.table("fwd_segs").reshape(-1, 4)
+def _forward_cover(wl, lim, fq, fs):
+    """(row, key) visit counts of the forward tables; asserts the per-segment rules."""
     cover = np.zeros((_stream_rows(wl), wl.tokens), dtype=np.int32)
     for tile in fq:
         rows, rl = _tile_rows(tile, lim)
@@ -198,16 +194,11 @@ def test_forward_schedule_covers_each_visible_pair_once(api, wl):
             else:
                 assert vis.all()  # an unmasked segment is below every row limit
             cover[rows[:, None], keys[None, :]] += vis
-    assert np.array_equal(cover, _expected_cover(wl))
+    return cover
 
 
-@pytest.mark.parametrize("wl", _schedule_cases(), ids=lambda w: w.name)
-def test_backward_schedule_covers_each_visible_pair_once(api, wl):
-    p = api.Plan.from_workload(wl)
-    lim = p.table("row_limit")
-    bq = p.table("bwd_qtiles").reshape(-1, 10)
-    bkv = p.table("bwd_kvtiles").reshape(-1, 8)
-    br = p.table("bwd_qranges").reshape(-1, 4)
+def _backward_cover(wl, lim, bq, bkv, br):
+    """(row, key) visit counts of the backward tables."""
     cover = np.zeros((_stream_rows(wl), wl.tokens), dtype=np.int32)
     for k0, nkeys, pos0, qr0, nqr in bkv[:, :5]:
         assert 0 <= nkeys <= 128
@@ -222,4 +213,68 @@ def test_backward_schedule_covers_each_visible_pair_once(api, wl):
                 if not diag:
                     assert vis.all()
                 cover[rows[:, None], keys[None, :]] += vis
-    assert np.array_equal(cover, _expected_cover(wl))
+    return cover
+
+
+def _fwd_tables(p):
+    return p.table("row_limit"), p.table("fwd_qtiles").reshape(-1, 10), p.table("fwd_segs").reshape(-1, 4)
+
+
+def _bwd_tables(p):
+    return (p.table("row_limit"), p.table("bwd_qtiles").reshape(-1, 10), p.table("bwd_kvtiles").reshape(-1, 8),
+            p.table("bwd_qranges").reshape(-1, 4))
+
+
+@pytest.mark.parametrize("wl", _schedule_cases(), ids=lambda w: w.name)
+def test_forward_schedule_covers_each_visible_pair_once(api, wl):
+    p = api.Plan.from_workload(wl)
+    assert np.array_equal(_forward_cover(wl, *_fwd_tables(p)), _expected_cover(wl))
+
+
+@pytest.mark.parametrize("wl", _schedule_cases(), ids=lambda w: w.name)
+def test_backward_schedule_covers_each_visible_pair_once(api, wl):
+    p = api.Plan.from_workload(wl)
+    assert np.array_equal(_backward_cover(wl, *_bwd_tables(p)), _expected_cover(wl))
+
+
+def _schedule_check_fails(fn):
+    try:
+        return not fn()
+    except AssertionError:
+        return True
+
+
+def test_schedule_checks_catch_planted_mistakes(api):
+    """Each planted table mistake (in a copy of the tables, on the host) makes
+    the coverage checks fail, so they would catch it in the planner."""
+    wl = W.small("ttt", [1280, 768], heads_q=8, heads_kv=2, head_dim=128, cp=2, depth=2, seed=7)
+    p = api.Plan.from_workload(wl)
+    want = _expected_cover(wl)
+    lim, fq, fs = _fwd_tables(p)
+    ok = lambda lim_, fq_, fs_: np.array_equal(_forward_cover(wl, lim_, fq_, fs_), want)
+    assert ok(lim, fq, fs)
+    # a segment dropped from a tile's list
+    fq2 = fq.copy()
+    t = int(np.argmax(fq2[:, 3]))
+    fq2[t, 3] -= 1
+    assert _schedule_check_fails(lambda: ok(lim, fq2, fs))
+    # a diagonal segment marked unmasked
+    fs2 = fs.copy()
+    fs2[np.nonzero(fs2[:, 3])[0][0], 3] = 0
+    assert _schedule_check_fails(lambda: ok(lim, fq, fs2))
+    # a segment shifted by one key
+    fs3 = fs.copy()
+    fs3[0, 2] += 1
+    assert _schedule_check_fails(lambda: ok(lim, fq, fs3))
+    lim, bq, bkv, br = _bwd_tables(p)
+    okb = lambda bkv_, br_: np.array_equal(_backward_cover(wl, lim, bq, bkv_, br_), want)
+    assert okb(bkv, br)
+    # a key tile that loses its last query range
+    bkv2 = bkv.copy()
+    t = int(np.argmax(bkv2[:, 4]))
+    bkv2[t, 4] -= 1
+    assert _schedule_check_fails(lambda: okb(bkv2, br))
+    # a key tile one key short
+    bkv3 = bkv.copy()
+    bkv3[np.nonzero(bkv3[:, 1])[0][0], 1] -= 1
+    assert _schedule_check_fails(lambda: okb(bkv3, br))
