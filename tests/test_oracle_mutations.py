@@ -91,3 +91,37 @@ def test_wrong_zigzag_owner_is_caught(monkeypatch):
     table = oracle.zigzag.chunk_table(np.array([0, 256]), 2)
     rows = [r for r in P.parse_golden(os.path.join(os.path.dirname(__file__), "golden", "zigzag_c2_L256.txt")) if r[0] != "packed"]
     assert any(int(r[3]) != t[4] for r, t in zip(rows, table))
+
+
+def _anchor_golden():
+    rows = P.parse_golden(os.path.join(os.path.dirname(__file__), "golden", "zigzag_anchors_c2.txt"))
+    ints = lambda tok: np.array([int(x) for x in tok.split(";")], dtype=np.int64)
+    return [(ints(r[1]), ints(r[2]), ints(r[3])) for r in rows]
+
+
+def test_anchors_left_in_natural_order_are_caught(monkeypatch):
+    monkeypatch.setattr(oracle.zigzag, "packed_anchor_order",
+                        lambda cu, C, anchors: np.arange(len(anchors)))
+    assert any(not np.array_equal(oracle.zigzag.packed_anchor_order(cu, 2, a), want)
+               for cu, a, want in _anchor_golden())
+
+
+def test_tail_chunk_before_head_chunk_is_caught(monkeypatch):
+    # rank-major, but each rank's tail chunk (2C-1-r) listed before its head chunk (r)
+    def wrong(cu, C, anchors):
+        chunk, owner = oracle.zigzag.token_chunk(cu, C)
+        a = np.asarray(anchors)
+        seq = np.searchsorted(np.asarray(cu), a, side="right") - 1
+        head = (chunk[a] == owner[a]).astype(np.int64)
+        return np.lexsort((a, head, seq, owner[a]))
+
+    monkeypatch.setattr(oracle.zigzag, "packed_anchor_order", wrong)
+    assert any(not np.array_equal(oracle.zigzag.packed_anchor_order(cu, 2, a), want)
+               for cu, a, want in _anchor_golden())
+
+
+def test_reversed_ring_direction_is_caught(monkeypatch):
+    monkeypatch.setattr(oracle.zigzag, "ring_source", lambda r, s, C: (r + s) % C)
+    rows = [[int(x) for x in r] for r in
+            P.parse_golden(os.path.join(os.path.dirname(__file__), "golden", "ring_c4.txt"))]
+    assert any([oracle.zigzag.ring_source(r, s, 4) for r in range(4)] != src for s, *src in rows)

@@ -156,6 +156,30 @@ def test_zigzag_golden():
     assert np.array_equal(perm, want)
 
 
+def _anchor_cases():
+    out = []
+    for r in P.parse_golden(os.path.join(GOLDEN, "zigzag_anchors_c2.txt")):
+        ints = lambda tok: np.array([int(x) for x in tok.split(";")], dtype=np.int64)
+        out.append((r[0], ints(r[1]), ints(r[2]), ints(r[3]), ints(r[4])))
+    return out
+
+
+@pytest.mark.parametrize("case", _anchor_cases(), ids=lambda c: c[0])
+def test_packed_anchor_order_golden(case):
+    _, cu, anchors, want_order, want_lim = case
+    order = oracle.zigzag.packed_anchor_order(cu, 2, anchors)
+    assert np.array_equal(order, want_order)
+    # every packed anchor's rows are limited at the anchor's own position
+    assert np.array_equal(anchors[order], want_lim)
+
+
+def test_ring_source_golden():
+    rows = [[int(x) for x in r] for r in P.parse_golden(os.path.join(GOLDEN, "ring_c4.txt"))]
+    assert [r[0] for r in rows] == [0, 1, 2, 3]
+    for s, *src in rows:
+        assert [oracle.zigzag.ring_source(r, s, 4) for r in range(4)] == src
+
+
 def test_eq3_volume_golden_and_branch_independence():
     rows = P.parse_golden(os.path.join(GOLDEN, "eq3_volume.txt"))
     for T, C, hkv, d, want in [[int(x) for x in r] for r in rows]:

@@ -62,6 +62,19 @@ def test_zigzag_tables_match_oracle(api, wl):
     assert np.array_equal(p.table("row_limit"), lim)
 
 
+def test_anchor_tables_match_hand_worked_golden(api):
+    from tests import oracle_pins as P
+    rows = P.parse_golden(os.path.join(ROOT, "tests", "golden", "zigzag_anchors_c2.txt"))
+    for r in rows:
+        ints = lambda tok: np.array([int(x) for x in tok.split(";")], dtype=np.int32)
+        cu, anchors, order, lim = ints(r[1]), ints(r[2]), ints(r[3]), ints(r[4])
+        S = len(cu) - 1
+        p = api.Plan("block", cu, 2, 1, 64, 2, block_size=3, anchors=anchors)
+        assert len(anchors) % S == 0
+        assert np.array_equal(p.table("anchor_perm"), order)
+        assert np.array_equal(p.table("row_limit"), np.repeat(lim, 3))
+
+
 @pytest.mark.parametrize("wl", _cases(), ids=lambda w: w.name)
 def test_useful_pairs_and_eq3_match_oracle(api, wl):
     p = api.Plan.from_workload(wl)
