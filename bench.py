@@ -223,9 +223,8 @@ def host_cores():
 
 
 # GEMMs per (row, key) pair each main-attention kernel runs: forward S and PV;
-# fused backward (mma.sync) S, dP, dV, dK, dQ; split backward: key-stationary
-# S, dP, dV, dK and query-stationary S, dP, dQ.
-MAIN_KERNEL_GEMMS = {"main_fwd": 2, "main_bwd": 5, "main_bwd_kv": 4, "main_bwd_dq": 3}
+# backward: key-stationary S, dP, dV, dK and query-stationary S, dP, dQ.
+MAIN_KERNEL_GEMMS = {"main_fwd": 2, "main_bwd_kv": 4, "main_bwd_dq": 3}
 
 
 def kernel_bytes(wl, info, name):
@@ -238,8 +237,8 @@ def kernel_bytes(wl, info, name):
         return 2 * 2 * (R * d + 2 * T * wl.heads_kv * d + 2 * nbk * d)
     if name == "lse_merge":
         return R * (2 * d * 4 + 2 * 4) + R * (d * 2 + 4)
-    if name == "bwd_prep":  # read o, dO, lse; write the row record and zero the dQ row
-        return R * (2 * d * 2 + 4) + R * (16 + d * 4)
+    if name == "bwd_prep":  # read o, dO, lse; write the row record
+        return R * (2 * d * 2 + 4) + R * 16
     if name == "branch_fwd":  # read q, k_b, v_b and the main partial (O_m fp32, l_m); write o (bf16) and lse
         return R * d * 2 + 2 * nbk * d * 2 + R * (d * 4 + 4) + R * (d * 2 + 4)
     if name == "branch_bwd":
@@ -340,6 +339,10 @@ def run_ours(args, rank, world, local):
                         "peak_source": f"hbm_gbs ({peaks['source']})"}
     launches = sum(n for n, _ in kt.values())
 
+    extra = {}
+    if args.extras:
+        extra = run_extras(args, plan, wl, t, info, peaks, ws, o, lse, grads)
+
     e2e = None
     if args.e2e_steps > 0:
         e2e = run_e2e(args, plan, wl, t, info, world, ws, o, lse, grads)
@@ -377,7 +380,98 @@ def run_ours(args, rank, world, local):
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
+    line.update(extra)
     return line
+
+
+def _time_launches(fn, n, warm=1):
+    """Mean device time (ms) of ``fn`` over ``n`` calls on the current stream,
+    after ``warm`` untimed calls; CUDA events on that stream."""
+    import torch
+    for _ in range(warm):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(n):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def run_extras(args, plan, wl, t, info, peaks, ws, o, lse, grads):
+    """Measurements outside the timed fwd+bwd steps, on the same workload:
+    the 8-bit forward (its TFLOP/s against an fp8 peak of twice the measured
+    bf16 one: the nominal dense rates are 4.5 and 2.25 PFLOP/s) and the
+    memory-bound kernels that the step does not launch (the zigzag pack, folded
+    into the kernels' load coordinates, and the stand-alone Eq. 2 merge)."""
+    import torch
+    from branch_attention_speculative_gb300 import api
+    out = {}
+    # ---- 8-bit forward
+    f8 = None
+    try:
+        ws8 = torch.empty(plan.workspace_bytes_fp8, dtype=torch.uint8, device="cuda")
+    except RuntimeError as e:  # out of memory
+        ws8 = None
+        f8 = {"skipped": str(e).splitlines()[0]}
+    if ws8 is not None:
+        run = lambda: plan.forward_fp8(t["q_b"], t["k_m"], t["v_m"], t["k_b"], t["v_b"], o=o, lse=lse, workspace=ws8)
+        run()
+        torch.cuda.synchronize()
+        if plan.check_device_status(ws8) != 0:
+            raise RuntimeError("device status after the 8-bit forward")
+        plan.profile(True)
+        plan.profile_read()
+        ms = _time_launches(run, args.steps, warm=0)
+        kt = plan.profile_read()
+        plan.profile(False)
+        peak8 = 2.0 * peaks["bf16_tflops_sustained"]
+        main_f = 4.0 * wl.head_dim * info["main_pairs"]
+        km = kt.get("main_fwd_fp8", (1, float("nan")))
+        kmain = km[1] / max(km[0], 1)
+        f8 = {"value": info["fwd_flops"] / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_forward": ms,
+              "dtype": "e4m3 QK^T and PV, fp32 softmax / lse, bf16 in and out",
+              "main_kernel": {"name": "main_fwd_fp8", "ms_per_launch": kmain,
+                              "achieved": main_f / (kmain / 1e3) / 1e12, "unit": "TFLOP/s", "peak": peak8,
+                              "frac": main_f / (kmain / 1e3) / 1e12 / peak8,
+                              "peak_source": f"2 x bf16_tflops_sustained ({peaks['source']}); nominal fp8 / bf16 "
+                                             "dense ratio 4.5 / 2.25"},
+              "kernels": {k: {"launches": n, "ms_per_launch": v / max(n, 1)} for k, (n, v) in kt.items()}}
+    out["fp8_forward"] = f8
+    # ---- memory-bound kernels outside the step
+    mb = {}
+    hbm = peaks["hbm_gbs"]
+    ms = _time_launches(lambda: plan.zigzag_pack("query", t["q_b"], dst=grads["dq_b"], workspace=ws), 5)
+    by = 2 * t["q_b"].numel() * 2
+    mb["zigzag_pack"] = {"bytes_per_launch": by, "ms_per_launch": ms, "achieved": by / (ms / 1e3) / 1e9,
+                         "unit": "GB/s", "peak": hbm, "frac": by / (ms / 1e3) / 1e9 / hbm,
+                         "what": f"q_b {tuple(t['q_b'].shape)} bf16 into zigzag order (read + write)"}
+    if ws8 is not None:
+        rows, d = 1 << 24, wl.head_dim
+        buf = ws8[: 2 * rows * d * 4 + 2 * rows * 4].view(torch.float32)
+        om, ob = buf[: rows * d].view(rows, d), buf[rows * d: 2 * rows * d].view(rows, d)
+        lm, lb = buf[2 * rows * d: 2 * rows * d + rows], buf[2 * rows * d + rows:]
+        g = torch.Generator(device="cuda").manual_seed(5)
+        for x in (om, ob, lm, lb):
+            x.normal_(generator=g)
+        res = {}
+
+        def merge():
+            res["o"] = api.lse_merge(om, lm, ob, lb)
+
+        ms = _time_launches(merge, 5)
+        by = rows * (2 * d * 4 + 2 * 4) + rows * (d * 2 + 4)
+        mb["lse_merge"] = {"bytes_per_launch": by, "ms_per_launch": ms, "achieved": by / (ms / 1e3) / 1e9,
+                           "unit": "GB/s", "peak": hbm, "frac": by / (ms / 1e3) / 1e9 / hbm,
+                           "what": f"Eq. 2 over {rows} rows x {d}: fp32 partials in, bf16 o and fp32 lse out "
+                                   "(includes the output allocation of the binding)"}
+        del res
+    out["memory_bound"] = mb
+    del ws8
+    torch.cuda.empty_cache()
+    return out
 
 
 def resize_workload(wl, tokens: int):
@@ -607,6 +701,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="skip the 8-bit forward and memory-bound kernel measurements")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling only: shrink the main sequence to this many tokens")
     args = ap.parse_args()

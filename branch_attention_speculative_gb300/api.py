@@ -88,6 +88,10 @@ _SIGS = {
     "ba_workspace_bytes": (ctypes.c_size_t, [_P]),
     "ba_forward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "ba_backward": (ctypes.c_int, [_P] + [_P] * 14 + [ctypes.c_size_t, _P]),
+    "ba_workspace_bytes_fp8": (ctypes.c_size_t, [_P]),
+    "ba_forward_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "ba_forward_step": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "ba_backward_step": (ctypes.c_int, [_P, ctypes.c_int32] + [_P] * 14 + [ctypes.c_size_t, _P]),
     "ba_check_device_status": (ctypes.c_int, [_P, _P, _P]),
     "ba_zigzag_pack": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "ba_lse_merge": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P]),
@@ -262,6 +266,28 @@ class Plan:
         _check(rc, "ba_forward")
         return o, lse
 
+    @property
+    def workspace_bytes_fp8(self) -> int:
+        return int(lib().ba_workspace_bytes_fp8(self._h))
+
+    def forward_fp8(self, q_b, k_m, v_m, k_b=None, v_b=None, o=None, lse=None, workspace=None, stream=None):
+        """Forward with the main part's QK^T and PV on e4m3 copies (per-tensor
+        scales) -> (o bf16, lse fp32); the workspace must hold
+        ``workspace_bytes_fp8`` bytes."""
+        self._check_inputs(q_b, k_m, v_m, k_b, v_b)
+        if o is None:
+            o = torch.empty_like(q_b)
+        if lse is None:
+            lse = torch.empty(q_b.shape[:-1], dtype=torch.float32, device=q_b.device)
+        _want(o, self.q_shape(), torch.bfloat16, "o")
+        _want(lse, self.q_shape()[:-1], torch.float32, "lse")
+        if workspace is None:
+            workspace = torch.empty(max(self.workspace_bytes_fp8, 256), dtype=torch.uint8, device=q_b.device)
+        rc = lib().ba_forward_fp8(self._h, _ptr(q_b), _ptr(k_m), _ptr(v_m), _ptr(k_b), _ptr(v_b), _ptr(o), _ptr(lse),
+                                  _ptr(workspace), workspace.numel(), _stream(stream))
+        _check(rc, "ba_forward_fp8")
+        return o, lse
+
     def forward_noalloc(self, q_b, k_m, v_m, k_b=None, v_b=None, o=None, lse=None, stream=None):
         """Forward through ba_forward_noalloc: the library's static scratch array
         replaces the workspace (plans up to 64 MiB of workspace).  Outputs must
@@ -300,6 +326,60 @@ class Plan:
                                workspace.numel(), _stream(stream))
         _check(rc, "ba_backward")
         return grads
+
+    # ---- EAGLE-3 TTT one step at a time
+    def step_shape(self):
+        return (self.T, self.heads_q, self.head_dim)
+
+    def forward_step(self, step: int, q_s, k_m, v_m, k_b, v_b, o=None, lse=None, workspace=None, stream=None):
+        """TTT step ``step`` alone -> (o_s, lse_s); q_s is that step's [T, Hq, d]
+        slice, k_b / v_b the whole [D, T, Hkv, d] buffers (slots > step unread)."""
+        if self.family != "ttt":
+            raise ValueError("forward_step needs a TTT plan")
+        _want(q_s, self.step_shape(), torch.bfloat16, "q_s")
+        _want(k_m, self.km_shape(), torch.bfloat16, "k_m")
+        _want(v_m, self.km_shape(), torch.bfloat16, "v_m")
+        _want(k_b, self.kb_shape(), torch.bfloat16, "k_b")
+        _want(v_b, self.kb_shape(), torch.bfloat16, "v_b")
+        if o is None:
+            o = torch.empty_like(q_s)
+        if lse is None:
+            lse = torch.empty(q_s.shape[:-1], dtype=torch.float32, device=q_s.device)
+        _want(o, self.step_shape(), torch.bfloat16, "o")
+        _want(lse, self.step_shape()[:-1], torch.float32, "lse")
+        if workspace is None:
+            workspace = self.workspace(q_s.device)
+        rc = lib().ba_forward_step(self._h, int(step), _ptr(q_s), _ptr(k_m), _ptr(v_m), _ptr(k_b), _ptr(v_b),
+                                   _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream))
+        _check(rc, "ba_forward_step")
+        return o, lse
+
+    def backward_step(self, step: int, q_s, k_m, v_m, k_b, v_b, o_s, lse_s, d_o_s, acc, dq=None, workspace=None,
+                      stream=None):
+        """Backward of TTT step ``step``: returns dq_s (bf16) and adds the
+        step's key gradients into ``acc`` (fp32 dk_m, dv_m, dk_b, dv_b)."""
+        if self.family != "ttt":
+            raise ValueError("backward_step needs a TTT plan")
+        for t, n in ((q_s, "q_s"), (o_s, "o_s"), (d_o_s, "d_o_s")):
+            _want(t, self.step_shape(), torch.bfloat16, n)
+        _want(lse_s, self.step_shape()[:-1], torch.float32, "lse_s")
+        _want(k_m, self.km_shape(), torch.bfloat16, "k_m")
+        _want(v_m, self.km_shape(), torch.bfloat16, "v_m")
+        _want(k_b, self.kb_shape(), torch.bfloat16, "k_b")
+        _want(v_b, self.kb_shape(), torch.bfloat16, "v_b")
+        for n, shape in (("dk_m", self.km_shape()), ("dv_m", self.km_shape()), ("dk_b", self.kb_shape()),
+                         ("dv_b", self.kb_shape())):
+            _want(acc[n], shape, torch.float32, n)
+        if dq is None:
+            dq = torch.empty_like(q_s)
+        if workspace is None:
+            workspace = self.workspace(q_s.device)
+        rc = lib().ba_backward_step(self._h, int(step), _ptr(q_s), _ptr(k_m), _ptr(v_m), _ptr(k_b), _ptr(v_b),
+                                    _ptr(o_s), _ptr(lse_s), _ptr(d_o_s), _ptr(dq), _ptr(acc["dk_m"]),
+                                    _ptr(acc["dv_m"]), _ptr(acc["dk_b"]), _ptr(acc["dv_b"]), _ptr(workspace),
+                                    workspace.numel(), _stream(stream))
+        _check(rc, "ba_backward_step")
+        return dq
 
     def profile(self, enable: bool = True):
         """Turn per-kernel event timing of this plan's launches on or off."""

@@ -3,7 +3,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <type_traits>
@@ -23,19 +22,6 @@ int cuda_fail(cudaError_t e) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool ok_tensor(const void* p) { return p != nullptr && aligned(p, 16); }
-
-// BA_MAIN_FWD=mma selects the mma.sync main forward (kept as the measured
-// baseline of the tcgen05 kernel); anything else runs the tcgen05 kernel.
-bool use_mma_fwd() {
-  const char* v = std::getenv("BA_MAIN_FWD");
-  return v && std::strcmp(v, "mma") == 0;
-}
-
-// Same for the backward (BA_MAIN_BWD=mma); head_dim 64 always takes mma.sync.
-bool use_mma_bwd(const BaShape& sh) {
-  const char* v = std::getenv("BA_MAIN_BWD");
-  return (v && std::strcmp(v, "mma") == 0) || !ba_main_bwd_tc_supported(sh);
-}
 
 unsigned char* ws_at(void* ws, size_t off) { return static_cast<unsigned char*>(ws) + off; }
 
@@ -111,10 +97,12 @@ cudaError_t pack(const ba_plan* p, const BaTables& tb, int role, const void* src
   } while (0)
 
 enum KernelId {
-  K_PACK = 0, K_MAIN_FWD, K_BRANCH_FWD, K_MERGE, K_BWD_PREP, K_MAIN_BWD, K_MAIN_BWD_DQ, K_BRANCH_BWD, K_COUNT
+  K_PACK = 0, K_MAIN_FWD, K_BRANCH_FWD, K_MERGE, K_BWD_PREP, K_MAIN_BWD, K_MAIN_BWD_DQ, K_BRANCH_BWD,
+  K_FP8_QUANT, K_MAIN_FWD_FP8, K_COUNT
 };
-const char* const kKernelNames[K_COUNT] = {"zigzag_pack", "main_fwd",    "branch_fwd", "lse_merge",
-                                           "bwd_prep",    "main_bwd_kv", "main_bwd_dq", "branch_bwd"};
+const char* const kKernelNames[K_COUNT] = {"zigzag_pack", "main_fwd",    "branch_fwd",   "lse_merge",
+                                           "bwd_prep",    "main_bwd_kv", "main_bwd_dq",  "branch_bwd",
+                                           "fp8_quantize", "main_fwd_fp8"};
 
 // Records an event pair around one launch when profiling is on.
 template <class F>
@@ -138,6 +126,115 @@ cudaError_t timed(ba_plan* p, int kid, cudaStream_t st, F&& launch) {
   p->prof_kernel.push_back(kid);
   p->prof_used = i + 1;
   return cudaSuccess;
+}
+
+// Output pointers of a backward call: bf16 gradients, or (single-step calls)
+// fp32 accumulators for the key gradients.
+struct BwdOut {
+  void *dq, *dkm, *dvm, *dkb, *dvb;
+  float *dkm_acc, *dvm_acc, *dkb_acc, *dvb_acc;
+};
+
+// The shape one TTT step runs with: one query step, global slot `step`, whose
+// queries read branch key slots 0..step.
+int step_shape(const ba_plan* p, int32_t step, BaShape* sh) {
+  if (!p || p->shape.family != BA_FAMILY_TTT || step < 0 || step >= p->shape.steps) return BA_ERR_INVALID_ARG;
+  *sh = p->shape;
+  sh->steps = 1;
+  sh->step0 = step;
+  sh->nbk = step + 1;
+  return BA_OK;
+}
+
+int run_forward(ba_plan* p, const BaShape& sh, const void* q_b, const void* k_m, const void* v_m, const void* k_b,
+                const void* v_b, void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream,
+                bool fp8 = false) {
+  const bool has_b = sh.family != BA_FAMILY_CAUSAL;
+  if (!ok_tensor(q_b) || !ok_tensor(k_m) || !ok_tensor(v_m) || !ok_tensor(o) || !ok_tensor(lse))
+    return BA_ERR_INVALID_ARG;
+  if (has_b && (!ok_tensor(k_b) || !ok_tensor(v_b))) return BA_ERR_INVALID_ARG;
+  if (fp8 && !p->fp8_ok) return BA_ERR_UNSUPPORTED;
+  if (int rc = check_ws(p, workspace, workspace_bytes)) return rc;
+  if (fp8 && workspace_bytes < p->ws.total_fp8) return BA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const BaWorkspaceLayout& w = p->ws;
+  BA_TRY(prepare(p, workspace, st));
+  BaFwdArgs a{};
+  a.sh = sh;
+  a.tb = device_tables(p, workspace);
+  a.q = q_b;
+  a.km = k_m;
+  a.vm = v_m;
+  a.kb = k_b;
+  a.vb = v_b;
+  a.om = reinterpret_cast<float*>(ws_at(workspace, w.om));
+  a.lm = reinterpret_cast<float*>(ws_at(workspace, w.lm));
+  a.o = o;
+  a.lse = lse;
+  if (fp8) {
+    float* amax = reinterpret_cast<float*>(ws_at(workspace, w.f8_amax));
+    a.q8 = ws_at(workspace, w.f8_q);
+    a.k8 = ws_at(workspace, w.f8_k);
+    a.vt8 = ws_at(workspace, w.f8_vt);
+    a.f8amax = amax;
+    BA_TRY(timed(p, K_FP8_QUANT, st, [&] {
+      return ba_launch_fp8_quantize(a, amax, const_cast<void*>(a.q8), const_cast<void*>(a.k8),
+                                    const_cast<void*>(a.vt8), st);
+    }));
+    BA_TRY(timed(p, K_MAIN_FWD_FP8, st, [&] { return ba_launch_main_fwd_fp8(a, st); }));
+  } else {
+    BA_TRY(timed(p, K_MAIN_FWD, st, [&] { return ba_launch_main_fwd_tc(a, st); }));
+  }
+  // with branches, the branch kernel merges each row with the main part (Eq.
+  // 2) and writes o and lse; without, the main partial passes through the
+  // merge pass
+  if (has_b && sh.nbk > 0 && sh.units > 0)
+    BA_TRY(timed(p, K_BRANCH_FWD, st, [&] { return ba_launch_branch_fwd(a, st); }));
+  else
+    BA_TRY(timed(p, K_MERGE, st, [&] { return ba_launch_merge_plan(a, st); }));
+  return BA_OK;
+}
+
+int run_backward(ba_plan* p, const BaShape& sh, const void* q_b, const void* k_m, const void* v_m, const void* k_b,
+                 const void* v_b, const void* o, const float* lse, const void* d_o, const BwdOut& out,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  const bool has_b = sh.family != BA_FAMILY_CAUSAL;
+  if (!ok_tensor(q_b) || !ok_tensor(k_m) || !ok_tensor(v_m) || !ok_tensor(o) || !ok_tensor(lse) ||
+      !ok_tensor(d_o) || !ok_tensor(out.dq) || !ok_tensor(out.dkm) || !ok_tensor(out.dvm))
+    return BA_ERR_INVALID_ARG;
+  if (has_b && (!ok_tensor(k_b) || !ok_tensor(v_b) || !ok_tensor(out.dkb) || !ok_tensor(out.dvb)))
+    return BA_ERR_INVALID_ARG;
+  if (int rc = check_ws(p, workspace, workspace_bytes)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const BaWorkspaceLayout& w = p->ws;
+  BA_TRY(prepare(p, workspace, st));
+  BaBwdArgs a{};
+  a.sh = sh;
+  a.tb = device_tables(p, workspace);
+  a.q = q_b;
+  a.km = k_m;
+  a.vm = v_m;
+  a.kb = k_b;
+  a.vb = v_b;
+  a.o = o;
+  a.d_o = d_o;
+  a.lse = lse;
+  a.rowrec = reinterpret_cast<float4*>(ws_at(workspace, w.rowrec));
+  a.dqacc = reinterpret_cast<float*>(ws_at(workspace, w.dqacc));
+  a.dq = out.dq;
+  a.dkm = out.dkm;
+  a.dvm = out.dvm;
+  a.dkb = out.dkb;
+  a.dvb = out.dvb;
+  a.dkm_acc = out.dkm_acc;
+  a.dvm_acc = out.dvm_acc;
+  a.dkb_acc = out.dkb_acc;
+  a.dvb_acc = out.dvb_acc;
+  BA_TRY(timed(p, K_BWD_PREP, st, [&] { return ba_launch_bwd_prep(a, st); }));
+  BA_TRY(timed(p, K_MAIN_BWD, st, [&] { return ba_launch_main_bwd_kv_tc(a, st); }));
+  BA_TRY(timed(p, K_MAIN_BWD_DQ, st, [&] { return ba_launch_main_bwd_q_tc(a, st); }));
+  BA_TRY(timed(p, K_BRANCH_BWD, st, [&] { return ba_launch_branch_bwd(a, st); }));
+  return BA_OK;
 }
 
 }  // namespace
@@ -247,79 +344,42 @@ size_t ba_workspace_bytes(ba_plan_t p) { return p ? p->ws.total : 0; }
 int ba_forward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, const void* k_b, const void* v_b,
                void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   if (!p) return BA_ERR_INVALID_ARG;
-  const bool has_b = p->shape.family != BA_FAMILY_CAUSAL;
-  if (!ok_tensor(q_b) || !ok_tensor(k_m) || !ok_tensor(v_m) || !ok_tensor(o) || !ok_tensor(lse))
-    return BA_ERR_INVALID_ARG;
-  if (has_b && (!ok_tensor(k_b) || !ok_tensor(v_b))) return BA_ERR_INVALID_ARG;
-  if (int rc = check_ws(p, workspace, workspace_bytes)) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const BaWorkspaceLayout& w = p->ws;
-  BA_TRY(prepare(p, workspace, st));
-  BaFwdArgs a{};
-  a.sh = p->shape;
-  a.tb = device_tables(p, workspace);
-  a.q = q_b;
-  a.km = k_m;
-  a.vm = v_m;
-  a.kb = k_b;
-  a.vb = v_b;
-  a.om = reinterpret_cast<float*>(ws_at(workspace, w.om));
-  a.lm = reinterpret_cast<float*>(ws_at(workspace, w.lm));
-  a.o = o;
-  a.lse = lse;
-  BA_TRY(timed(p, K_MAIN_FWD, st,
-               [&] { return use_mma_fwd() ? ba_launch_main_fwd(a, st) : ba_launch_main_fwd_tc(a, st); }));
-  // with branches, the branch kernel merges each row with the main part (Eq.
-  // 2) and writes o and lse; without, the main partial passes through the
-  // merge pass
-  if (has_b && p->shape.nbk > 0 && p->shape.units > 0)
-    BA_TRY(timed(p, K_BRANCH_FWD, st, [&] { return ba_launch_branch_fwd(a, st); }));
-  else
-    BA_TRY(timed(p, K_MERGE, st, [&] { return ba_launch_merge_plan(a, st); }));
-  return BA_OK;
+  return run_forward(p, p->shape, q_b, k_m, v_m, k_b, v_b, o, lse, workspace, workspace_bytes, stream);
 }
 
 int ba_backward(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, const void* k_b, const void* v_b,
                 const void* o, const float* lse, const void* d_o, void* dq_b, void* dk_m, void* dv_m, void* dk_b,
                 void* dv_b, void* workspace, size_t workspace_bytes, void* stream) {
   if (!p) return BA_ERR_INVALID_ARG;
-  const bool has_b = p->shape.family != BA_FAMILY_CAUSAL;
-  if (!ok_tensor(q_b) || !ok_tensor(k_m) || !ok_tensor(v_m) || !ok_tensor(o) || !ok_tensor(lse) ||
-      !ok_tensor(d_o) || !ok_tensor(dq_b) || !ok_tensor(dk_m) || !ok_tensor(dv_m))
+  const BwdOut out{dq_b, dk_m, dv_m, dk_b, dv_b, nullptr, nullptr, nullptr, nullptr};
+  return run_backward(p, p->shape, q_b, k_m, v_m, k_b, v_b, o, lse, d_o, out, workspace, workspace_bytes, stream);
+}
+
+size_t ba_workspace_bytes_fp8(ba_plan_t p) { return p ? p->ws.total_fp8 : 0; }
+
+int ba_forward_fp8(ba_plan_t p, const void* q_b, const void* k_m, const void* v_m, const void* k_b, const void* v_b,
+                   void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!p) return BA_ERR_INVALID_ARG;
+  return run_forward(p, p->shape, q_b, k_m, v_m, k_b, v_b, o, lse, workspace, workspace_bytes, stream, true);
+}
+
+int ba_forward_step(ba_plan_t p, int32_t step, const void* q_s, const void* k_m, const void* v_m, const void* k_b,
+                    const void* v_b, void* o_s, float* lse_s, void* workspace, size_t workspace_bytes, void* stream) {
+  BaShape sh;
+  if (int rc = step_shape(p, step, &sh)) return rc;
+  return run_forward(p, sh, q_s, k_m, v_m, k_b, v_b, o_s, lse_s, workspace, workspace_bytes, stream);
+}
+
+int ba_backward_step(ba_plan_t p, int32_t step, const void* q_s, const void* k_m, const void* v_m, const void* k_b,
+                     const void* v_b, const void* o_s, const float* lse_s, const void* d_o_s, void* dq_s,
+                     float* dk_m_acc, float* dv_m_acc, float* dk_b_acc, float* dv_b_acc, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  BaShape sh;
+  if (int rc = step_shape(p, step, &sh)) return rc;
+  if (!ok_tensor(dk_m_acc) || !ok_tensor(dv_m_acc) || !ok_tensor(dk_b_acc) || !ok_tensor(dv_b_acc))
     return BA_ERR_INVALID_ARG;
-  if (has_b && (!ok_tensor(k_b) || !ok_tensor(v_b) || !ok_tensor(dk_b) || !ok_tensor(dv_b)))
-    return BA_ERR_INVALID_ARG;
-  if (int rc = check_ws(p, workspace, workspace_bytes)) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const BaWorkspaceLayout& w = p->ws;
-  BA_TRY(prepare(p, workspace, st));
-  BaBwdArgs a{};
-  a.sh = p->shape;
-  a.tb = device_tables(p, workspace);
-  a.q = q_b;
-  a.km = k_m;
-  a.vm = v_m;
-  a.kb = k_b;
-  a.vb = v_b;
-  a.o = o;
-  a.d_o = d_o;
-  a.lse = lse;
-  a.rowrec = reinterpret_cast<float4*>(ws_at(workspace, w.rowrec));
-  a.dqacc = reinterpret_cast<float*>(ws_at(workspace, w.dqacc));
-  a.dq = dq_b;
-  a.dkm = dk_m;
-  a.dvm = dv_m;
-  a.dkb = dk_b;
-  a.dvb = dv_b;
-  BA_TRY(timed(p, K_BWD_PREP, st, [&] { return ba_launch_bwd_prep(a, st); }));
-  if (use_mma_bwd(a.sh)) {
-    BA_TRY(timed(p, K_MAIN_BWD, st, [&] { return ba_launch_main_bwd(a, st); }));
-  } else {
-    BA_TRY(timed(p, K_MAIN_BWD, st, [&] { return ba_launch_main_bwd_kv_tc(a, st); }));
-    BA_TRY(timed(p, K_MAIN_BWD_DQ, st, [&] { return ba_launch_main_bwd_q_tc(a, st); }));
-  }
-  BA_TRY(timed(p, K_BRANCH_BWD, st, [&] { return ba_launch_branch_bwd(a, st); }));
-  return BA_OK;
+  const BwdOut out{dq_s, dk_m_acc, dv_m_acc, dk_b_acc, dv_b_acc, dk_m_acc, dv_m_acc, dk_b_acc, dv_b_acc};
+  return run_backward(p, sh, q_s, k_m, v_m, k_b, v_b, o_s, lse_s, d_o_s, out, workspace, workspace_bytes, stream);
 }
 
 int ba_check_device_status(ba_plan_t p, void* workspace, void* stream) {

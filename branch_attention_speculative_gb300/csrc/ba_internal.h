@@ -12,9 +12,10 @@
 #define BA_BWD_BM 64    // query rows per backward query tile
 #define BA_BWD_BN 128   // keys per backward key tile
 #define BA_BWD_CS 4     // key tiles per thread-block cluster of the dK/dV kernel:
-                        // the tiles of a cluster come from one chunk, meet the
-                        // same query tiles in the same order and share each
-                        // Q / dO tile through one multicast load
+                        // the tiles of a cluster come from one chunk and meet
+                        // the same query tiles in the same order; the cluster
+                        // only makes them run side by side, so each CTA's own
+                        // loads of a Q / dO tile follow the first one into L2
 
 // Device status word values (first word of the workspace).
 #define BA_DEV_OK 0u
@@ -73,7 +74,10 @@ struct BaShape {
   int32_t d;
   int32_t steps;      // D for TTT, 1 otherwise (leading dim of q_b)
   int32_t B;          // block size (BLOCK), 1 otherwise
-  int32_t nbk;        // branch keys per unit: D (TTT), B (BLOCK), 0 (CAUSAL)
+  int32_t nbk;        // branch key slots a unit's queries read: D (TTT), B (BLOCK),
+                      // 0 (CAUSAL); step + 1 in a single-step TTT call
+  int32_t step0;      // TTT: slot of the call's first query step (0 for the
+                      // whole plan; the step in a single-step call)
   int64_t T;          // main tokens
   int64_t rows;       // packed rows per stream: T (TTT/CAUSAL) or NA * B (BLOCK)
   int64_t units;      // anchor units: T (TTT/CAUSAL) or NA (BLOCK)

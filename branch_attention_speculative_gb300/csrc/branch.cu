@@ -45,8 +45,10 @@ __device__ __forceinline__ void unit_query(const BaShape& sh, int64_t u, int qi,
   else { j = 0; r = u; }
 }
 
+// branch keys of query qi of a unit: the step-j TTT query sees slots 0..j
+// (j = step0 + qi, its global step), a block query all B keys of its block
 __device__ __forceinline__ int keys_of_query(const BaShape& sh, int qi) {
-  return sh.family == BA_FAMILY_TTT ? qi + 1 : (sh.family == BA_FAMILY_BLOCK ? sh.B : 0);
+  return sh.family == BA_FAMILY_TTT ? sh.step0 + qi + 1 : (sh.family == BA_FAMILY_BLOCK ? sh.B : 0);
 }
 
 template <int D>
@@ -110,12 +112,16 @@ __device__ void stage_keys(const BaShape& sh, const __nv_bfloat16* kb, const __n
 }
 
 // dK_b / dV_b of one unit and kv head from shared memory (fp32) to their bf16
-// key slots.  16-byte stores of 8 values.
+// key slots (16-byte stores of 8 values), or added into the fp32 accumulators
+// of a single-step call (each slot of a unit and kv head belongs to one CTA,
+// so the read-add-write needs no atomics).
 template <int D>
-__device__ void store_key_grads(const BaShape& sh, __nv_bfloat16* dkb, __nv_bfloat16* dvb, int64_t u, int kvh,
-                                const float* dks, const float* dvs) {
+__device__ void store_key_grads(const BaShape& sh, const BaBwdArgs& a, int64_t u, int kvh, const float* dks,
+                                const float* dvs) {
   constexpr int CH = D / 8;
   const int n = sh.nbk * CH;
+  auto* dkb = static_cast<__nv_bfloat16*>(a.dkb);
+  auto* dvb = static_cast<__nv_bfloat16*>(a.dvb);
   for (int e = threadIdx.x; e < 2 * n; e += blockDim.x) {
     const int m = e >= n ? 1 : 0;
     const int ee = e - m * n;
@@ -123,8 +129,15 @@ __device__ void store_key_grads(const BaShape& sh, __nv_bfloat16* dkb, __nv_bflo
     const int64_t off = (branch_slot(sh, u, i) * sh.Hkv + kvh) * D + c * 8;
     const float4* src = reinterpret_cast<const float4*>((m ? dvs : dks) + i * D + c * 8);
     const float4 x = src[0], y = src[1];
-    *reinterpret_cast<uint4*>((m ? dvb : dkb) + off) =
-        make_uint4(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w), pack_bf16(y.x, y.y), pack_bf16(y.z, y.w));
+    if (a.dkb_acc) {
+      float4* acc = reinterpret_cast<float4*>((m ? a.dvb_acc : a.dkb_acc) + off);
+      const float4 p = acc[0], q = acc[1];
+      acc[0] = make_float4(p.x + x.x, p.y + x.y, p.z + x.z, p.w + x.w);
+      acc[1] = make_float4(q.x + y.x, q.y + y.y, q.z + y.z, q.w + y.w);
+    } else {
+      *reinterpret_cast<uint4*>((m ? dvb : dkb) + off) =
+          make_uint4(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w), pack_bf16(y.x, y.y), pack_bf16(y.z, y.w));
+    }
   }
 }
 
@@ -221,8 +234,6 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
   const auto* kb = static_cast<const __nv_bfloat16*>(a.kb);
   const auto* vb = static_cast<const __nv_bfloat16*>(a.vb);
   auto* dq = static_cast<__nv_bfloat16*>(a.dq);
-  auto* dkb = static_cast<__nv_bfloat16*>(a.dkb);
-  auto* dvb = static_cast<__nv_bfloat16*>(a.dvb);
   const int64_t total = sh.units * sh.Hkv;
   const int nq = rows_per_unit(sh) * sh.G;
   for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
@@ -314,7 +325,7 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
       }
     }
     __syncthreads();
-    store_key_grads<D>(sh, dkb, dvb, u, kvh, dks, dvs);
+    store_key_grads<D>(sh, a, u, kvh, dks, dvs);
   }
 }
 

@@ -15,6 +15,10 @@ struct BaFwdArgs {
   float *om, *lm;                     // main partials (fp32, workspace)
   void* o;                            // output (bf16)
   float* lse;                         // lse (fp32)
+  // 8-bit forward: e4m3 copies of q, k_m and V^T ([Hkv][d][T]) in the
+  // workspace and the amax of q, k_m, v_m (each scale = amax / 448)
+  const void *q8, *k8, *vt8;
+  const float* f8amax;
 };
 
 struct BaBwdArgs {
@@ -26,6 +30,9 @@ struct BaBwdArgs {
   float4* rowrec;                     // per (step, head, row), stream-major: {lse*log2e, Delta, limit, 0}
   float* dqacc;                       // fp32 dQ accumulator, like q_b (workspace)
   void *dq, *dkm, *dvm, *dkb, *dvb;   // gradients (bf16)
+  // single-step TTT calls: the key gradients are added into these fp32
+  // accumulators (natural layouts) instead of being written to dkm .. dvb
+  float *dkm_acc, *dvm_acc, *dkb_acc, *dvb_acc;
 };
 
 // K1: dst[o][i] = src[o][perm[i]] (inverse = 0) or dst[o][perm[i]] = src[o][i].
@@ -37,10 +44,15 @@ inline cudaError_t set_dynamic_smem(Kernel* kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
 }
 
-// K2: causal main attention over each query tile's key segments -> O_m, l_m.
-// tcgen05 / TMEM / TMA kernel (the default) and the mma.sync kernel it replaces.
+// K2: causal main attention over each query tile's key segments -> O_m, l_m
+// (tcgen05 / TMEM / TMA; head_dim 64 and 128).
 cudaError_t ba_launch_main_fwd_tc(const BaFwdArgs& a, cudaStream_t st);
-cudaError_t ba_launch_main_fwd(const BaFwdArgs& a, cudaStream_t st);
+// K2 with 8-bit operands (head_dim 128): QK^T and PV on e4m3 copies.
+cudaError_t ba_launch_main_fwd_fp8(const BaFwdArgs& a, cudaStream_t st);
+// Quantisation for it: amax of q, k_m, v_m (into amax[3], zeroed first), then
+// the e4m3 copies q8, k8 and the transposed vt8 [Hkv][d][T].
+cudaError_t ba_launch_fp8_quantize(const BaFwdArgs& a, float* amax, void* q8, void* k8, void* vt8,
+                                   cudaStream_t st);
 // K3 + K4: rank-local branch attention, each row merged with O_m, l_m by
 // Eq. 2 as it is computed -> o, lse.
 cudaError_t ba_launch_branch_fwd(const BaFwdArgs& a, cudaStream_t st);
@@ -49,15 +61,13 @@ cudaError_t ba_launch_merge_plan(const BaFwdArgs& a, cudaStream_t st);
 // K4 on caller buffers.
 cudaError_t ba_launch_merge_rows(int64_t rows, int d, const float* om, const float* lm, const float* ob,
                                  const float* lb, void* o, float* l, cudaStream_t st);
-// K5: Delta = rowsum(dO * O) and the row records; zeroes the dQ accumulator.
+// K5: Delta = rowsum(dO * O) and the row records.
 cudaError_t ba_launch_bwd_prep(const BaBwdArgs& a, cudaStream_t st);
-// K6: main-attention backward (key-stationary): dK_m, dV_m (natural), dQ into the accumulator.
-// tcgen05 path (head_dim 128): key-stationary dK/dV kernel + query-stationary dQ
-// kernel; and the mma.sync kernel (any head_dim; the baseline, dQ by atomics).
-bool ba_main_bwd_tc_supported(const BaShape& sh);
+// K6: main-attention backward on tcgen05 (head_dim 64 and 128): the
+// key-stationary kernel writes dK_m, dV_m (natural order); the
+// query-stationary kernel writes every row of the fp32 dQ accumulator.
 cudaError_t ba_launch_main_bwd_kv_tc(const BaBwdArgs& a, cudaStream_t st);
 cudaError_t ba_launch_main_bwd_q_tc(const BaBwdArgs& a, cudaStream_t st);
-cudaError_t ba_launch_main_bwd(const BaBwdArgs& a, cudaStream_t st);
 // K7 (+K8): branch backward: dK_b, dV_b (natural); dQ = accumulator + branch part -> natural bf16.
 cudaError_t ba_launch_branch_bwd(const BaBwdArgs& a, cudaStream_t st);
 

@@ -28,6 +28,11 @@
 // Warps: 0-7 compute (warp w: TMEM lane quarter w % 4 = query rows, keys
 // 64 (w / 4) .. of each block; two warps per SM sub-partition hide each other's
 // latencies), 8 TMA, 9 MMA + TMEM.
+// head_dim 64 and 128: the kernel is templated on d (tiles of d / 64
+// 128-byte swizzled blocks; dQ takes d TMEM columns).
+// Every query row of the plan lies in exactly one tile and every tile writes
+// all of its rows (zeros for a tile without key blocks), so the accumulator
+// needs no clearing beforehand.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -44,13 +49,15 @@ constexpr int NTHREADS = 320;  // 8 compute warps, 1 TMA warp, 1 MMA warp
 constexpr int NK = 3;          // K ring stages
 constexpr int NV = 2;          // V ring stages
 
+template <int D>
 struct DqSmem {
+  static constexpr int CB = D / 64;              // 64-column (128-byte) blocks per row
   static constexpr uint32_t TILE = 128u * 128u;  // [128 rows][64 columns] bf16, swizzled
-  static constexpr uint32_t q = 0;               // 2 blocks
-  static constexpr uint32_t go = q + 2 * TILE;   // 2 blocks
-  static constexpr uint32_t k = go + 2 * TILE;       // [NK stages][2 blocks]
-  static constexpr uint32_t v = k + NK * 2 * TILE;   // [NV stages][2 blocks]
-  static constexpr uint32_t bars = v + NV * 2 * TILE;
+  static constexpr uint32_t q = 0;               // CB blocks
+  static constexpr uint32_t go = q + CB * TILE;  // CB blocks
+  static constexpr uint32_t k = go + CB * TILE;       // [NK stages][CB blocks]
+  static constexpr uint32_t v = k + NK * CB * TILE;   // [NV stages][CB blocks]
+  static constexpr uint32_t bars = v + NV * CB * TILE;
   static constexpr uint32_t bytes = bars + 256;
   static constexpr uint32_t alloc = bytes + 1024;
 };
@@ -93,12 +100,13 @@ struct BlockIter {
   }
 };
 
+template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
     main_bwd_q_tc_kernel(const BaBwdArgs a, const __grid_constant__ CUtensorMap tmq,
                          const __grid_constant__ CUtensorMap tmdo, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
-  using L = DqSmem;
-  constexpr int D = 128;
+  using L = DqSmem<D>;
+  constexpr int CB = L::CB;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -162,8 +170,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
       const int qrow = int(int64_t(j) * sh.rows + tile.nrow0);
-      mbar_expect_tx(bar(B_QFULL), 4 * L::TILE);
-      for (int cb = 0; cb < 2; ++cb) {
+      mbar_expect_tx(bar(B_QFULL), 2 * CB * L::TILE);
+      for (int cb = 0; cb < CB; ++cb) {
         tma_load_3d(sbase + L::q + cb * L::TILE, &tmq, bar(B_QFULL), cb * 64, h, qrow);
         tma_load_3d(sbase + L::go + cb * L::TILE, &tmdo, bar(B_QFULL), cb * 64, h, qrow);
       }
@@ -173,13 +181,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int ks = i % NK, vs = i % NV;
         const int key = it.cur.pos0 + it.kb;  // natural key row
         if (!mbar_wait(bar(B_VEMPTY + vs), ((i / NV) & 1) ^ 1, tb.status, abort_flag)) break;
-        mbar_expect_tx(bar(B_VFULL + vs), 2 * L::TILE);
-        for (int cb = 0; cb < 2; ++cb)
-          tma_load_3d(sbase + L::v + (vs * 2 + cb) * L::TILE, &tmv, bar(B_VFULL + vs), cb * 64, kvh, key);
+        mbar_expect_tx(bar(B_VFULL + vs), CB * L::TILE);
+        for (int cb = 0; cb < CB; ++cb)
+          tma_load_3d(sbase + L::v + (vs * CB + cb) * L::TILE, &tmv, bar(B_VFULL + vs), cb * 64, kvh, key);
         if (!mbar_wait(bar(B_KEMPTY + ks), ((i / NK) & 1) ^ 1, tb.status, abort_flag)) break;
-        mbar_expect_tx(bar(B_KFULL + ks), 2 * L::TILE);
-        for (int cb = 0; cb < 2; ++cb)
-          tma_load_3d(sbase + L::k + (ks * 2 + cb) * L::TILE, &tmk, bar(B_KFULL + ks), cb * 64, kvh, key);
+        mbar_expect_tx(bar(B_KFULL + ks), CB * L::TILE);
+        for (int cb = 0; cb < CB; ++cb)
+          tma_load_3d(sbase + L::k + (ks * CB + cb) * L::TILE, &tmk, bar(B_KFULL + ks), cb * 64, kvh, key);
       }
     }
   } else if (warp == 9) {
@@ -199,7 +207,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
-          tc_mma(tDP, desc_add(dg0, off), desc_add(dv0, vs * 2 * L::TILE + off), id_s, kk > 0);
+          tc_mma(tDP, desc_add(dg0, off), desc_add(dv0, vs * CB * L::TILE + off), id_s, kk > 0);
         }
         tc_commit(bar(B_VEMPTY + vs));
         return true;
@@ -212,7 +220,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
-          tc_mma(tS + sb * KBN, desc_add(dq0, off), desc_add(dk0, ks * 2 * L::TILE + off), id_s, kk > 0);
+          tc_mma(tS + sb * KBN, desc_add(dq0, off), desc_add(dk0, ks * CB * L::TILE + off), id_s, kk > 0);
         }
         tc_commit(bar(B_SFULL + sb));  // also covers dP(i), issued before
         return true;
@@ -221,7 +229,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int ks = i % NK, sb = i & 1;
         if (!mbar_wait(bar(B_DSFULL + sb), (i >> 1) & 1, tb.status, abort_flag)) return false;
         tc_fence_after();
-        const uint64_t dks = desc_add(dkm, ks * 2 * L::TILE);
+        const uint64_t dks = desc_add(dkm, ks * CB * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < KBN / 16; ++kk)
           tc_mma_tmem_a(tDQ, tS + sb * KBN + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(dks, kk * 2048), id_q,
@@ -308,16 +316,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(bar(B_DSFULL + sb));
     }
     // epilogue: dQ (main part, scaled) -> fp32 accumulator row, written once;
-    // each warp writes d-columns 64 (w / 4) .. of its 32 rows
-    if (ok && i > 0 && mbar_wait_warp(bar(B_SFREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, tb.status, abort_flag)) {
-      tc_fence_after();
+    // each warp writes d-columns (d / 2) (w / 4) .. of its 32 rows (zeros when
+    // the tile has no key blocks)
+    constexpr int HD = D / 2;
+    const bool have = ok && i > 0 &&
+                      mbar_wait_warp(bar(B_SFREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, tb.status, abort_flag);
+    if (have || (ok && i == 0)) {
+      if (have) tc_fence_after();
       const int64_t qrow = (int64_t(j) * sh.rows + tile.nrow0 + r) * sh.Hq + h;
-      float4* dst = reinterpret_cast<float4*>(a.dqacc + qrow * D + half * 64);
+      float4* dst = reinterpret_cast<float4*>(a.dqacc + qrow * D + half * HD);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < HD / 32; ++c) {
         float o[32];
-        tmem_ld32(tDQ + lane_off + half * 64 + c * 32, o);
-        tmem_wait_ld();
+        if (have) {
+          tmem_ld32(tDQ + lane_off + half * HD + c * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
         if (rok) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -357,9 +374,9 @@ cudaError_t encoder() {
   return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
-cudaError_t map3d(CUtensorMap* m, const void* base, int heads, int64_t rows) {
-  const cuuint64_t dims[3] = {128, cuuint64_t(heads), cuuint64_t(rows)};
-  const cuuint64_t strides[2] = {256, cuuint64_t(heads) * 256};
+cudaError_t map3d(CUtensorMap* m, const void* base, int d, int heads, int64_t rows) {
+  const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
+  const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(heads) * d * 2};
   const cuuint32_t box[3] = {64, 1, 128};
   const cuuint32_t es[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -368,24 +385,30 @@ cudaError_t map3d(CUtensorMap* m, const void* base, int heads, int64_t rows) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+template <int D>
+cudaError_t launch_q(const BaBwdArgs& a, int64_t grid, cudaStream_t st) {
+  const int64_t qrows = int64_t(a.sh.steps) * a.sh.rows;
+  CUtensorMap mq, mdo, mk, mv;
+  cudaError_t e;
+  if ((e = map3d(&mq, a.q, D, a.sh.Hq, qrows)) != cudaSuccess) return e;
+  if ((e = map3d(&mdo, a.d_o, D, a.sh.Hq, qrows)) != cudaSuccess) return e;
+  if ((e = map3d(&mk, a.km, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  if ((e = map3d(&mv, a.vm, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  const int smem = int(DqSmem<D>::alloc);
+  if ((e = cudaFuncSetAttribute(main_bwd_q_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+      cudaSuccess)
+    return e;
+  main_bwd_q_tc_kernel<D><<<unsigned(grid), NTHREADS, smem, st>>>(a, mq, mdo, mk, mv);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t ba_launch_main_bwd_q_tc(const BaBwdArgs& a, cudaStream_t st) {
   const int64_t grid = int64_t(a.tb.n_fq) * a.sh.steps * a.sh.Hq;
   if (grid == 0) return cudaSuccess;
-  if (grid > 0x7fffffffLL || a.sh.d != 128) return cudaErrorInvalidConfiguration;
+  if (grid > 0x7fffffffLL || (a.sh.d != 128 && a.sh.d != 64)) return cudaErrorInvalidConfiguration;
   cudaError_t e = encoder();
   if (e != cudaSuccess) return e;
-  const int64_t qrows = int64_t(a.sh.steps) * a.sh.rows;
-  CUtensorMap mq, mdo, mk, mv;
-  if ((e = map3d(&mq, a.q, a.sh.Hq, qrows)) != cudaSuccess) return e;
-  if ((e = map3d(&mdo, a.d_o, a.sh.Hq, qrows)) != cudaSuccess) return e;
-  if ((e = map3d(&mk, a.km, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
-  if ((e = map3d(&mv, a.vm, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
-  const int smem = int(DqSmem::alloc);
-  if ((e = cudaFuncSetAttribute(main_bwd_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
-      cudaSuccess)
-    return e;
-  main_bwd_q_tc_kernel<<<unsigned(grid), NTHREADS, smem, st>>>(a, mq, mdo, mk, mv);
-  return cudaGetLastError();
+  return a.sh.d == 128 ? launch_q<128>(a, grid, st) : launch_q<64>(a, grid, st);
 }

@@ -32,7 +32,19 @@
 // queued on the tensor cores behind the current PV while the softmax runs.
 // Every wait is bounded (BA_WAIT_CYCLES); a timeout records BA_DEV_TIMEOUT,
 // every role leaves its loop, and TMEM is released before the CTA exits.
+//
+// 8-bit variant (F8 = true; rainbus page, limitations and future work, item
+// (4): fp8 training of the decomposition).  Q, K and V^T arrive as e4m3
+// copies with per-tensor scales (s_q, s_k, s_v = amax / 448, made by the
+// quantisation kernels); QK^T and PV run as kind::f8f6f4 MMAs with K = 32,
+// S is fp32 in TMEM, the softmax folds s_q s_k into its scale and keeps the
+// row max, sum and lse in fp32, P (at most 2^8 by the lazy rescale) is stored
+// as e4m3, four per TMEM column, and the epilogue multiplies O by s_v.  A d =
+// 128 row of 8-bit values is one 128-byte swizzled block; V is read from its
+// transposed copy [Hkv][d][T], so the PV GEMM's B operand is K-major (keys
+// along the 128-byte rows) like every other operand.
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include <mutex>
@@ -48,9 +60,11 @@ constexpr int NTHREADS = 224;  // 4 softmax warps, 1 TMA warp, 2 MMA-issuing war
 constexpr int NKV = 3;    // K / V ring stages
 constexpr int NSB = 3;    // S (and P) buffers in TMEM
 
-template <int D>
+template <int D, bool F8>
 struct FwdSmem {
-  static constexpr int CB = D / 64;                       // 64-column (128-byte) blocks per row
+  static constexpr int EB = F8 ? 1 : 2;                   // bytes per element
+  static constexpr int CB = D * EB / 128;                 // 128-byte blocks per row
+  static constexpr int ELB = 128 / EB;                    // elements per block row
   static constexpr uint32_t TILE = 128u * 128u;           // one 128-row x 128-byte swizzled block
   static constexpr uint32_t q = 0;
   static constexpr uint32_t k = q + CB * TILE;            // [NKV stages][CB blocks]
@@ -111,11 +125,22 @@ __device__ __forceinline__ void load_scores(float (&s)[TBN], uint32_t taddr, boo
   }
 }
 
-template <int D>
+// Four fp32 values as e4m3, packed low byte first (the element order of a
+// K-major 8-bit operand along a TMEM column).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+// Per-tensor fp8 scale from an amax (amax / 448, or 1 for an all-zero tensor).
+__device__ __forceinline__ float f8_scale(float amax) { return amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f; }
+
+template <int D, bool F8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     main_fwd_tc_kernel(const BaFwdArgs a, const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-  using L = FwdSmem<D>;
+  using L = FwdSmem<D, F8>;
   constexpr int CB = L::CB;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -178,7 +203,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_prefetch_desc(&tmv);
       mbar_expect_tx(bar(B_QFULL), CB * L::TILE);
       for (int cb = 0; cb < CB; ++cb)
-        tma_load_3d(sbase + L::q + cb * L::TILE, &tmq, bar(B_QFULL), cb * 64, h, int(j * sh.rows + tile.nrow0));
+        tma_load_3d(sbase + L::q + cb * L::TILE, &tmq, bar(B_QFULL), cb * L::ELB, h, int(j * sh.rows + tile.nrow0));
       BlockIter it;
       it.init(tb.fseg, tile.seg0, tile.nseg);
       for (int i = 0; it.valid(); ++i, it.next()) {
@@ -188,30 +213,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(bar(B_KEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
         mbar_expect_tx(bar(B_KFULL + st), CB * L::TILE);
         for (int cb = 0; cb < CB; ++cb)
-          tma_load_3d(sbase + L::k + (st * CB + cb) * L::TILE, &tmk, bar(B_KFULL + st), cb * 64, kvh, key);
+          tma_load_3d(sbase + L::k + (st * CB + cb) * L::TILE, &tmk, bar(B_KFULL + st), cb * L::ELB, kvh, key);
         if (!mbar_wait(bar(B_VEMPTY + st), ph ^ 1, tb.status, abort_flag)) break;
         mbar_expect_tx(bar(B_VFULL + st), CB * L::TILE);
-        for (int cb = 0; cb < CB; ++cb)
-          tma_load_3d(sbase + L::v + (st * CB + cb) * L::TILE, &tmv, bar(B_VFULL + st), cb * 64, kvh, key);
+        if constexpr (F8) {
+          // V^T block: d rows of 128 keys (key a multiple of 16: the plan checks
+          // that every chunk starts on a 16-token boundary)
+          tma_load_3d(sbase + L::v + st * L::TILE, &tmv, bar(B_VFULL + st), key, 0, kvh);
+        } else {
+          for (int cb = 0; cb < CB; ++cb)
+            tma_load_3d(sbase + L::v + (st * CB + cb) * L::TILE, &tmv, bar(B_VFULL + st), cb * 64, kvh, key);
+        }
       }
     }
   } else if (warp == 5 || warp == 6) {
     // ------------------------------------------------------------ MMA issuers
     if (elect_one()) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, TBN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idesc_qk =
+          F8 ? idesc_e4m3_f32(128, TBN, false, false) : idesc_bf16_f32(128, TBN, false, false);
+      // 8-bit: V^T makes B K-major; 16-bit: V is an MN-major B
+      constexpr uint32_t idesc_pv = F8 ? idesc_e4m3_f32(128, D, false, false) : idesc_bf16_f32(128, D, false, true);
       // operand descriptors, built once: every MMA below adds a constant offset
       const uint64_t dq0 = smem_desc_sw128(sbase + L::q, 16, 1024), dk0 = smem_desc_sw128(sbase + L::k, 16, 1024);
-      const uint64_t dvm = smem_desc_sw128(sbase + L::v, L::TILE, 1024);
+      const uint64_t dvm = smem_desc_sw128(sbase + L::v, F8 ? 16 : L::TILE, 1024);
       auto issue_pv = [&](int i) -> bool {
         const int pb = i % NSB, vs = i % NKV;
         if (!mbar_wait(bar(B_PFULL + pb), (i / NSB) & 1, tb.status, abort_flag)) return false;
         if (!mbar_wait(bar(B_VFULL + vs), (i / NKV) & 1, tb.status, abort_flag)) return false;
         tc_fence_after();
         const uint64_t dvs = desc_add(dvm, vs * CB * L::TILE);
+        if constexpr (F8) {
+          // P: 32 keys per K step = 8 TMEM columns; V^T: 32 keys = 32 bytes along its rows
 #pragma unroll
-        for (int kk = 0; kk < TBN / 16; ++kk)
-          tc_mma_tmem_a(tO, tS + pb * TBN + kk * 8, desc_add(dvs, kk * 2048), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < TBN / 32; ++kk)
+            tc_mma_f8_tmem_a(tO, tS + pb * TBN + kk * 8, desc_add(dvs, kk * 32), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < TBN / 16; ++kk)
+            tc_mma_tmem_a(tO, tS + pb * TBN + kk * 8, desc_add(dvs, kk * 2048), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
         tc_commit(bar(B_SFREE + pb));
         tc_commit(bar(B_VEMPTY + vs));
         return true;
@@ -227,10 +267,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (!mbar_wait(bar(B_SFREE + sb), ((i / NSB) & 1) ^ 1, tb.status, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint64_t dks = desc_add(dk0, ks * CB * L::TILE);
+          if constexpr (F8) {
+            // a K = 32 step is 32 bytes along the single 128-byte block
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
-            tc_mma(tS + sb * TBN, desc_add(dq0, off), desc_add(dks, off), idesc_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 32; ++kk)
+              tc_mma_f8(tS + sb * TBN, desc_add(dq0, kk * 32), desc_add(dks, kk * 32), idesc_qk, kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * L::TILE + (kk & 3) * 32;
+              tc_mma(tS + sb * TBN, desc_add(dq0, off), desc_add(dks, off), idesc_qk, kk > 0 ? 1u : 0u);
+            }
           }
           tc_commit(bar(B_SFULL + sb));
           tc_commit(bar(B_KEMPTY + ks));
@@ -246,6 +293,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int lim = r < tile.nrows ? tb.row_lim[tile.row0 + r] : -1;
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
     float m_used = -INFINITY, l = 0.f;
+    // scores come out of the MMA in units of the operands: the 8-bit path
+    // folds the two quantisation scales into the softmax scale
+    const float sl2 = F8 ? sh.scale_log2 * f8_scale(a.f8amax[0]) * f8_scale(a.f8amax[1]) : sh.scale_log2;
+    // P of one 32-key group into its columns of the S buffer it came from:
+    // bf16 two per column (16 columns), e4m3 four per column (8 columns)
+    auto store_p = [&](const float* pv, uint32_t taddr_group0, int g) {
+      if constexpr (F8) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = pack_e4m3x4(pv[4 * e], pv[4 * e + 1], pv[4 * e + 2], pv[4 * e + 3]);
+        tmem_st8(taddr_group0 + g * 8, w);
+      } else {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = pack_bf16(pv[2 * e], pv[2 * e + 1]);
+        tmem_st16(taddr_group0 + g * 16, w);
+      }
+    };
     BlockIter it;
     it.init(tb.fseg, tile.seg0, tile.nseg);
     int i = 0;
@@ -273,7 +338,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float rsp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < TBN; ++c) {
-          s[c] = ex2_approx(fmaf(s[c], sh.scale_log2, -m_used));
+          s[c] = ex2_approx(fmaf(s[c], sl2, -m_used));
           rsp[c & 7] += s[c];
         }
         const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
@@ -284,10 +349,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           l += rs;
 #pragma unroll
           for (int g = 0; g < TBN / 32; ++g) {
-            uint32_t w[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) w[e] = pack_bf16(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
-            tmem_st16(tS + lane_off + sb * TBN + g * 16, w);
+            store_p(s + 32 * g, tS + lane_off + sb * TBN, g);
           }
         }
       }
@@ -301,7 +363,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) mxp[k] = fmaxf(mxp[k], mxp[k + 4]);
         const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
-        const float m_blk = mx * sh.scale_log2;
+        const float m_blk = mx * sl2;
         const bool grow = m_blk > m_used + 8.f;
         const float m_next = grow ? m_blk : m_used;
         const float base = m_next == -INFINITY ? 0.f : m_next;
@@ -336,13 +398,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int g = 0; g < TBN / 32; ++g) {
 #pragma unroll
           for (int c = 32 * g; c < 32 * g + 32; ++c) {
-            s[c] = ex2_approx(fmaf(s[c], sh.scale_log2, -base));
+            s[c] = ex2_approx(fmaf(s[c], sl2, -base));
             rsp[c & 7] += s[c];
           }
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = pack_bf16(s[32 * g + 2 * e], s[32 * g + 2 * e + 1]);
-          tmem_st16(tS + lane_off + sb * TBN + g * 16, w);
+          store_p(s + 32 * g, tS + lane_off + sb * TBN, g);
         }
         l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
       }
@@ -356,7 +415,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       const bool write = r < tile.nrows;
       const int64_t qrow = (int64_t(j) * sh.rows + tile.nrow0 + r) * sh.Hq + h;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? (F8 ? f8_scale(a.f8amax[2]) : 1.f) / l : 0.f;
       float4* dst = reinterpret_cast<float4*>(a.om + qrow * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -402,31 +461,51 @@ cudaError_t get_encoder() {
   return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
-// 3-D view (d, heads, rows) of a row-major [rows][heads][d] bf16 tensor; box (64, 1, 128).
-cudaError_t make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows) {
+// 3-D view (d, heads, rows) of a row-major [rows][heads][d] tensor of 1- or
+// 2-byte elements; box (128 bytes of d, 1, 128 rows).
+cudaError_t make_map(CUtensorMap* m, const void* base, int esize, int d, int heads, int64_t rows) {
   const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(heads), cuuint64_t(rows)};
-  const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(heads) * d * 2};
-  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint64_t strides[2] = {cuuint64_t(d) * esize, cuuint64_t(heads) * d * esize};
+  const cuuint32_t box[3] = {cuuint32_t(128 / esize), 1, 128};
   const cuuint32_t es[3] = {1, 1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+  const CUtensorMapDataType dt = esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D>
+// 3-D view (keys, d, kv heads) of the 8-bit V^T copy [Hkv][d][T]; box (128 keys, 128 d rows, 1).
+cudaError_t make_map_vt(CUtensorMap* m, const void* base, int d, int heads, int64_t T) {
+  const cuuint64_t dims[3] = {cuuint64_t(T), cuuint64_t(d), cuuint64_t(heads)};
+  const cuuint64_t strides[2] = {cuuint64_t(T), cuuint64_t(T) * d};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, bool F8>
 cudaError_t launch(const BaFwdArgs& a, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   cudaError_t e;
-  if ((e = make_map(&mq, a.q, D, a.sh.Hq, int64_t(a.sh.steps) * a.sh.rows)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.km, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.vm, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  const int es = F8 ? 1 : 2;
+  const int64_t qrows = int64_t(a.sh.steps) * a.sh.rows;
+  if ((e = make_map(&mq, F8 ? a.q8 : a.q, es, D, a.sh.Hq, qrows)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, F8 ? a.k8 : a.km, es, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  if constexpr (F8) {
+    if ((e = make_map_vt(&mv, a.vt8, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  } else {
+    if ((e = make_map(&mv, a.vm, es, D, a.sh.Hkv, a.sh.T)) != cudaSuccess) return e;
+  }
   const int64_t grid = int64_t(a.tb.n_fq) * a.sh.steps * a.sh.Hq;
-  const int smem = int(FwdSmem<D>::alloc);
-  if ((e = cudaFuncSetAttribute(main_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+  const int smem = int(FwdSmem<D, F8>::alloc);
+  if ((e = cudaFuncSetAttribute(main_fwd_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
       cudaSuccess)
     return e;
-  main_fwd_tc_kernel<D><<<unsigned(grid), NTHREADS, smem, st>>>(a, mq, mk, mv);
+  main_fwd_tc_kernel<D, F8><<<unsigned(grid), NTHREADS, smem, st>>>(a, mq, mk, mv);
   return cudaGetLastError();
 }
 
@@ -438,5 +517,15 @@ cudaError_t ba_launch_main_fwd_tc(const BaFwdArgs& a, cudaStream_t st) {
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e = get_encoder();
   if (e != cudaSuccess) return e;
-  return a.sh.d == 128 ? launch<128>(a, st) : launch<64>(a, st);
+  return a.sh.d == 128 ? launch<128, false>(a, st) : launch<64, false>(a, st);
+}
+
+cudaError_t ba_launch_main_fwd_fp8(const BaFwdArgs& a, cudaStream_t st) {
+  const int64_t grid = int64_t(a.tb.n_fq) * a.sh.steps * a.sh.Hq;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL || a.sh.d != 128 || !a.q8 || !a.k8 || !a.vt8 || !a.f8amax)
+    return cudaErrorInvalidConfiguration;
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  return launch<128, true>(a, st);
 }

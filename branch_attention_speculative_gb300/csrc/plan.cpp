@@ -101,6 +101,7 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
   sh.steps = fam == BA_FAMILY_TTT ? D : 1;
   sh.B = fam == BA_FAMILY_BLOCK ? B : 1;
   sh.nbk = fam == BA_FAMILY_TTT ? D : (fam == BA_FAMILY_BLOCK ? B : 0);
+  sh.step0 = 0;
   sh.T = T;
   sh.rows = rows;
   sh.units = fam == BA_FAMILY_BLOCK ? NA : T;
@@ -364,6 +365,15 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
   w.rowrec = b; b = align256(b + qrows * 16);
   w.dqacc = b; b = align256(b + qrows * dd * 4);
   w.total = std::max(f, b);
+  size_t g = align256(w.total);
+  w.f8_amax = g; g += 256;
+  w.f8_q = g; g = align256(g + qrows * dd);
+  w.f8_k = g; g = align256(g + size_t(T) * sh.Hkv * dd);
+  w.f8_vt = g; g = align256(g + size_t(T) * sh.Hkv * dd);
+  w.total_fp8 = g;
+  p->fp8_ok = sh.d == 128 && T % 16 == 0;
+  for (const BaChunk& ch : p->chunks)
+    if (ch.nat0 % 16 != 0) p->fp8_ok = false;
 
   // ---- host image of the table region
   try {

@@ -18,6 +18,10 @@ struct BaWorkspaceLayout {
   size_t om, lm;                  // forward main partials (fp32, natural order)
   size_t rowrec, dqacc;           // backward scratch: row records (16 B), dQ (fp32), natural order
   size_t total;
+  // 8-bit forward (after `total`, so it overlaps neither scratch region):
+  // amax[3], e4m3 copies of q and k_m, the transposed e4m3 V^T [Hkv][d][T]
+  size_t f8_amax, f8_q, f8_k, f8_vt;
+  size_t total_fp8;
 };
 
 // Chunk c of sequence s: natural start, packed start, length, owner rank.
@@ -51,6 +55,9 @@ struct ba_plan {
   std::vector<int64_t> comm;     // Eq. 3 bytes per rank
 
   int64_t main_pairs = 0, branch_pairs = 0, fwd_blocks = 0;
+  // the 8-bit forward's V^T loads start at chunk starts: they must be
+  // multiples of 16 tokens (TMA inner coordinate), and head_dim must be 128
+  bool fp8_ok = false;
 
   BaWorkspaceLayout ws;
   std::vector<unsigned char> image;  // host copy of the table region

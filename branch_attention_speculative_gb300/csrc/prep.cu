@@ -4,10 +4,10 @@
 // softmax backward, dS = P * (dP - Delta)).  lse (in base 2), Delta and the
 // row's main-key limit go into one 16-byte record per (step, head, row), in
 // natural row order and stream-major, so that the records of a query tile (a
-// run of consecutive natural rows) are one contiguous TMA box; the row of the
-// fp32 dQ accumulator is zeroed.  The pages only say that the backward replays the
-// ring ("Online Draft Co-Training ...", rainbus page, method step 5); Delta is
-// what that replay needs per row when P is recomputed from the merged lse.
+// run of consecutive natural rows) are one contiguous TMA box.  The pages only
+// say that the backward replays the ring ("Online Draft Co-Training ...",
+// rainbus page, method step 5); Delta is what that replay needs per row when P
+// is recomputed from the merged lse.
 // HBM-bound: d/8 threads per row, 16-byte loads.
 #include "device.cuh"
 #include "kernels.h"
@@ -47,9 +47,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BaBwdArgs a) {
 #pragma unroll
     for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
     if (!valid) continue;
-    float4* dq = reinterpret_cast<float4*>(a.dqacc + row * D);
-    dq[2 * sub] = make_float4(0.f, 0.f, 0.f, 0.f);
-    dq[2 * sub + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (sub == 0) {  // one 16-byte record per (step, head, row), stream-major
       const int64_t srow = (j * sh.Hq + h) * sh.rows + r;
       a.rowrec[srow] = make_float4(a.lse[row] * BA_LOG2E, acc, __int_as_float(a.tb.nat_lim[r]), 0.f);

@@ -121,8 +121,10 @@ typedef enum {
                                 limit when diag = 1                             */
   BA_TABLE_BWD_QTILES = 6,   /* [n][10] backward query tiles, fields as FWD_QTILES */
   BA_TABLE_BWD_KVTILES = 7,  /* [n][8] backward key tiles: {k0, nkeys, pos0, qr0,
-                                nqr, work, chunk, 0}; nkeys = 0 for the fillers
-                                that complete a cluster                         */
+                                nqr, work, chunk, 0}, in groups of four tiles of
+                                one chunk that share their query ranges (one
+                                thread-block cluster); nkeys = 0 for the fillers
+                                that complete a group                           */
   BA_TABLE_BWD_QRANGES = 8   /* [n][4] query-tile ranges of the key tiles, ring-
                                 replay order: {t0, t1, diag, 0} (BWD_QTILES
                                 indices t0 .. t1 - 1)                           */
@@ -160,10 +162,12 @@ int ba_plan_get_comm_volume(ba_plan_t plan, int64_t* out, int32_t capacity);
  * by two calls at once; consecutive calls may share it. */
 size_t ba_workspace_bytes(ba_plan_t plan);
 
-/* Forward (rainbus page, method step 2; Figure 1(b)).  Packs the inputs into
- * zigzag order, runs causal main attention over each query tile's key chunks
- * in ring order (online softmax merge between steps), rank-local branch
- * attention, and the Eq. 2 merge, which writes o and lse in natural order.
+/* Forward (rainbus page, method step 2; Figure 1(b)).  Runs causal main
+ * attention for each query tile over its key chunks in ring order, with the
+ * online-softmax merge between ring steps; the zigzag layout lives only in the
+ * plan's tile tables, so q_b, k_m and v_m are read in place (no packed
+ * copies).  Then rank-local branch attention, fused with the Eq. 2 merge of
+ * each row's two parts, writes o and lse in natural order.
  * Inputs q_b, k_m, v_m, k_b, v_b; outputs o (bf16) and lse (fp32). */
 int ba_forward(ba_plan_t plan, const void* q_b, const void* k_m, const void* v_m,
                const void* k_b, const void* v_b, void* o, float* lse,
@@ -179,6 +183,63 @@ int ba_backward(ba_plan_t plan, const void* q_b, const void* k_m, const void* v_
                 const void* k_b, const void* v_b, const void* o, const float* lse,
                 const void* d_o, void* dq_b, void* dk_m, void* dv_m, void* dk_b, void* dv_b,
                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Forward with 8-bit main attention (rainbus page, limitations and future
+ * work, item (4): extending the decomposition to fp8 training; the same page
+ * warns about precision at bf16 / fp8 beyond 256K).  Same inputs, outputs and
+ * key sets as ba_forward; the main part's QK^T and PV run on e4m3 copies of
+ * q_b, k_m and v_m with per-tensor scales (amax / 448, found on the device at
+ * every call), while the scores, the softmax, the row sums and the lse stay
+ * fp32 and the branch part and the Eq. 2 merge are computed as in ba_forward.
+ * Accuracy is that of e4m3 (3 mantissa bits): o agrees with the exact result
+ * to about 5-6% relative RMS on normally distributed inputs, and lse to a few
+ * hundredths.  Needs head_dim 128 and every zigzag chunk starting on a
+ * multiple of 16 tokens (BA_ERR_UNSUPPORTED otherwise), and a workspace of
+ * ba_workspace_bytes_fp8(plan) bytes, which holds the e4m3 copies. */
+size_t ba_workspace_bytes_fp8(ba_plan_t plan);
+int ba_forward_fp8(ba_plan_t plan, const void* q_b, const void* k_m, const void* v_m,
+                   const void* k_b, const void* v_b, void* o, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* EAGLE-3 TTT one step at a time (ai.info summary, Main Findings: the
+ * EAGLE-3 draft's training-time test runs its steps as separate passes, the
+ * queries, keys and values of a step being produced from the draft's output of
+ * the step before; rainbus page, core method: the branch keys of a step stay
+ * local to the anchor's rank).  For a TTT plan of depth D, `step` s in
+ * [0, D) is the step whose queries attend the causal main prefix [seq_start, p]
+ * and the branch keys (p, 0..s) of their position p.  Running steps 0..D-1
+ * through ba_forward_step gives the same o and lse, bit for bit, as one
+ * ba_forward over all D steps.
+ *   q_s, o_s        [T][Hq][d] bf16: step s's slice of q_b / o (any address,
+ *                   e.g. q_b + s*T*Hq*d)
+ *   lse_s           [T][Hq] fp32
+ *   k_b, v_b        the whole [D][T][Hkv][d] branch buffers: slots 0..s must
+ *                   hold their keys / values; slots above s are never read, so
+ *                   they may still be unwritten
+ *   k_m, v_m, workspace as for ba_forward (the plan's workspace size serves).
+ * Errors as ba_forward, and BA_ERR_INVALID_ARG for a plan that is not TTT or
+ * a step outside [0, D). */
+int ba_forward_step(ba_plan_t plan, int32_t step, const void* q_s, const void* k_m, const void* v_m,
+                    const void* k_b, const void* v_b, void* o_s, float* lse_s,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward of one TTT step (rainbus page, method step 5: the ring is replayed
+ * and gradients accumulate locally).  Given step s's q_s, o_s, lse_s and output
+ * gradient d_o_s (slices as in ba_forward_step), writes dq_s ([T][Hq][d] bf16)
+ * and ADDS step s's contributions into fp32 accumulators the caller owns:
+ *   dk_m_acc, dv_m_acc  [T][Hkv][d] fp32  (main keys: every step adds)
+ *   dk_b_acc, dv_b_acc  [D][T][Hkv][d] fp32  (slots 0..s receive this step's
+ *                       share; slots above s are not touched)
+ * Zero the accumulators before the first step of a backward pass; after all D
+ * steps (in any order) they hold the gradients ba_backward returns in bf16, up
+ * to rounding.  Steps that share accumulators must not overlap on the GPU.
+ * Errors as ba_backward, and BA_ERR_INVALID_ARG for a plan that is not TTT, a
+ * step outside [0, D) or a missing / misaligned accumulator. */
+int ba_backward_step(ba_plan_t plan, int32_t step, const void* q_s, const void* k_m, const void* v_m,
+                     const void* k_b, const void* v_b, const void* o_s, const float* lse_s,
+                     const void* d_o_s, void* dq_s, float* dk_m_acc, float* dv_m_acc,
+                     float* dk_b_acc, float* dv_b_acc, void* workspace, size_t workspace_bytes,
+                     void* stream);
 
 /* Synchronises `stream`, reads and clears the status word in `workspace`,
  * and returns the first device-side error recorded since the word was last
@@ -206,9 +267,16 @@ int ba_zigzag_pack(ba_plan_t plan, int32_t role, const void* src, void* dst, int
  * ba_workspace_bytes exceeds that limit are rejected with BA_ERR_WORKSPACE
  * before anything runs.  The first call on a device looks the array's device
  * address up (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls share the array and it keeps the
- * last call's contents (what must start at zero is cleared by each call);
- * calls that overlap on the GPU race on it, so order them.  No cudaMalloc,
+ * call before any stream capture.  The address is kept per device for the
+ * life of the process: after cudaDeviceReset (or anything else that tears the
+ * device's context down) this entry point must not be called again in that
+ * process.  All calls share the array and it keeps the last call's contents
+ * (what must start at zero is cleared by each call); calls that overlap on the
+ * GPU race on it, so order them.  The kernels' own fault reports (a bounded
+ * wait that ran out, a table index out of range) land in the status word of
+ * that hidden array, which no entry point reads back: on this path only launch
+ * errors are returned, and a caller that needs the device-side checks uses
+ * ba_forward with a workspace and ba_check_device_status.  No cudaMalloc,
  * cudaFree or other allocating routine is called. */
 #define BA_NOALLOC_SCRATCH_BYTES (64ull << 20)
 int ba_forward_noalloc(ba_plan_t plan, const void* q_b, const void* k_m, const void* v_m, const void* k_b,
@@ -240,7 +308,7 @@ int ba_lse_merge(int64_t rows, int32_t head_dim, const float* o_m, const float* 
  * recorded events, adds their elapsed times per kernel name since the last
  * read, writes up to `capacity` entries and returns the entry count in
  * *count.  Names: zigzag_pack, main_fwd, branch_fwd, lse_merge, bwd_prep,
- * main_bwd, branch_bwd. */
+ * main_bwd_kv, main_bwd_dq, branch_bwd, fp8_quantize, main_fwd_fp8. */
 typedef struct {
   char name[24];
   int64_t launches;

@@ -26,7 +26,7 @@ def api():
 def header_symbols():
     txt = open(os.path.join(ROOT, "include", "ba.h")).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-    return sorted(set(re.findall(r"\b(ba_[a-z_]+)\s*\(", txt)))
+    return sorted(set(re.findall(r"\b(ba_[a-z0-9_]+)\s*\(", txt)))
 
 
 def test_library_exports_every_header_symbol(api):
