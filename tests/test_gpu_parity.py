@@ -154,7 +154,11 @@ def test_config1_full_parity(api):
 # ---------------------------------------------------------------- measured shapes, sampled
 
 
-@pytest.mark.parametrize("k,n_units,window", [(2, 48, 64), (3, 32, 256), (4, 24, 256), (5, 24, 24)])
+# Main-key gradient windows at the end of the last sequence: at the 256K shape
+# one whole 128-key tile, whose attending query rows sit more than 2^31
+# elements into q_b; at the 128K block shape four tiles, one cluster of the
+# dK/dV kernel.
+@pytest.mark.parametrize("k,n_units,window", [(2, 48, 64), (3, 32, 256), (4, 24, 512), (5, 24, 128)])
 def test_config_sampled_parity(api, k, n_units, window):
     wl = W.config(k)
     t = W.make_tensors(wl, device="cuda")
