@@ -97,12 +97,10 @@ cudaError_t pack(const ba_plan* p, const BaTables& tb, int role, const void* src
   } while (0)
 
 enum KernelId {
-  K_PACK = 0, K_MAIN_FWD, K_BRANCH_FWD, K_MERGE, K_BWD_PREP, K_MAIN_BWD, K_MAIN_BWD_DQ, K_BRANCH_BWD,
-  K_FP8_QUANT, K_MAIN_FWD_FP8, K_COUNT
+  K_PACK = 0, K_MAIN_FWD, K_BWD_PREP, K_MAIN_BWD, K_MAIN_BWD_DQ, K_BRANCH_BWD, K_FP8_QUANT, K_MAIN_FWD_FP8, K_COUNT
 };
-const char* const kKernelNames[K_COUNT] = {"zigzag_pack", "main_fwd",    "branch_fwd",   "lse_merge",
-                                           "bwd_prep",    "main_bwd_kv", "main_bwd_dq",  "branch_bwd",
-                                           "fp8_quantize", "main_fwd_fp8"};
+const char* const kKernelNames[K_COUNT] = {"zigzag_pack", "main_fwd",   "bwd_prep",     "main_bwd_kv",
+                                           "main_bwd_dq", "branch_bwd", "fp8_quantize", "main_fwd_fp8"};
 
 // Records an event pair around one launch when profiling is on.
 template <class F>
@@ -167,8 +165,6 @@ int run_forward(ba_plan* p, const BaShape& sh, const void* q_b, const void* k_m,
   a.vm = v_m;
   a.kb = k_b;
   a.vb = v_b;
-  a.om = reinterpret_cast<float*>(ws_at(workspace, w.om));
-  a.lm = reinterpret_cast<float*>(ws_at(workspace, w.lm));
   a.o = o;
   a.lse = lse;
   if (fp8) {
@@ -185,13 +181,8 @@ int run_forward(ba_plan* p, const BaShape& sh, const void* q_b, const void* k_m,
   } else {
     BA_TRY(timed(p, K_MAIN_FWD, st, [&] { return ba_launch_main_fwd_tc(a, st); }));
   }
-  // with branches, the branch kernel merges each row with the main part (Eq.
-  // 2) and writes o and lse; without, the main partial passes through the
-  // merge pass
-  if (has_b && sh.nbk > 0 && sh.units > 0)
-    BA_TRY(timed(p, K_BRANCH_FWD, st, [&] { return ba_launch_branch_fwd(a, st); }));
-  else
-    BA_TRY(timed(p, K_MERGE, st, [&] { return ba_launch_merge_plan(a, st); }));
+  // the main kernel's epilogue adds each row's branch part by Eq. 2 and
+  // writes o and lse: nothing else runs
   return BA_OK;
 }
 
@@ -220,7 +211,6 @@ int run_backward(ba_plan* p, const BaShape& sh, const void* q_b, const void* k_m
   a.d_o = d_o;
   a.lse = lse;
   a.rowrec = reinterpret_cast<float4*>(ws_at(workspace, w.rowrec));
-  a.dqacc = reinterpret_cast<float*>(ws_at(workspace, w.dqacc));
   a.dq = out.dq;
   a.dkm = out.dkm;
   a.dvm = out.dvm;

@@ -1,4 +1,4 @@
-// K3 / K7 — rank-local branch attention, forward and backward.
+// K7 — rank-local branch attention, backward: the branch keys' gradients.
 //
 // "Online Draft Co-Training ...", ai.info summary, Key Contributions 1 and
 // "Methodology in Plain English": the branch part is small and lives on the
@@ -9,18 +9,17 @@
 //   BLOCK — each of the B queries of an anchor sees all B keys of the block.
 //
 // One CTA handles one anchor unit (a token position for TTT, an anchor for
-// BLOCK; natural order, since the branch part needs no zigzag) and one kv head: the unit's few branch keys are staged in shared
-// memory as fp32, each warp takes query rows, a lane owns d/32 columns, dot
-// products are warp-shuffle reductions.  The work is tiny next to the main
-// part and bound by HBM traffic of q, dO and the outputs.
+// BLOCK; natural order, since the branch part needs no zigzag) and one kv
+// head: the unit's few branch keys are staged in shared memory as fp32, each
+// warp takes query rows, a lane owns d/32 columns, dot products are
+// warp-shuffle reductions, and dK_b / dV_b of the unit are summed over all of
+// its rows (every step and q head of the group) before one store.  The work is
+// tiny next to the main part and bound by HBM traffic of q and dO.
 //
-// The forward also finishes the output: each row's branch part is merged with
-// the main part by Eq. 2 as soon as it is computed, so neither O_b nor a
-// separate merge pass over the rows touches HBM.
-//
-// The backward also finishes dQ: the main part arrives in the fp32
-// accumulator, the branch part is added here and the sum is written as bf16
-// in natural order (the finalize step, fused).
+// The forward's branch part and Eq. 2 merge, and the branch part of dQ, are
+// computed per row in the epilogues of the main-attention kernels, which own
+// those rows; only the key gradients, which sum over rows of many CTAs there,
+// are gathered here.
 #include <math.h>
 
 #include "device.cuh"
@@ -64,32 +63,7 @@ __device__ __forceinline__ void load_row(const __nv_bfloat16* p, int lane, float
   }
 }
 
-template <int D>
-__device__ __forceinline__ void load_row_f32(const float* p, int lane, float* x) {
-  constexpr int E = D / 32;
-  if constexpr (E == 4) {
-    const float4 v = reinterpret_cast<const float4*>(p)[lane];
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-  } else {
-    const float2 v = reinterpret_cast<const float2*>(p)[lane];
-    x[0] = v.x; x[1] = v.y;
-  }
-}
-
 constexpr int NKR = 8;  // branch keys per unit whose gradients a warp keeps in registers
-
-template <int D>
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* p, int lane, const float* x) {
-  constexpr int E = D / 32;
-  if constexpr (E == 4) {
-    uint2 v;
-    v.x = pack_bf16(x[0], x[1]);
-    v.y = pack_bf16(x[2], x[3]);
-    reinterpret_cast<uint2*>(p)[lane] = v;
-  } else {
-    reinterpret_cast<uint32_t*>(p)[lane] = pack_bf16(x[0], x[1]);
-  }
-}
 
 // One unit's branch keys of one kv head into shared memory as fp32: row i of
 // ks / vs is key slot branch_slot(u, i).  16-byte loads of 8 values.
@@ -142,84 +116,6 @@ __device__ void store_key_grads(const BaShape& sh, const BaBwdArgs& a, int64_t u
 }
 
 template <int D>
-__global__ void __launch_bounds__(128) branch_fwd_kernel(BaFwdArgs a) {
-  extern __shared__ float smem[];
-  constexpr int E = D / 32;
-  const BaShape& sh = a.sh;
-  float* ks = smem;
-  float* vs = smem + sh.nbk * D;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const auto* qg = static_cast<const __nv_bfloat16*>(a.q);
-  const auto* kb = static_cast<const __nv_bfloat16*>(a.kb);
-  const auto* vb = static_cast<const __nv_bfloat16*>(a.vb);
-  const int64_t total = sh.units * sh.Hkv;
-  const int nq = rows_per_unit(sh) * sh.G;
-  for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-    const int64_t u = w / sh.Hkv;
-    const int kvh = int(w % sh.Hkv);
-    __syncthreads();
-    stage_keys<D>(sh, kb, vb, u, kvh, ks, vs);
-    __syncthreads();
-    for (int idx = warp; idx < nq; idx += nwarps) {
-      const int qi = idx / sh.G, g = idx % sh.G;
-      int64_t j, r;
-      unit_query(sh, u, qi, j, r);
-      const int64_t qrow = (j * sh.rows + r) * sh.Hq + kvh * sh.G + g;
-      float q[E], acc[E];
-      load_row<D>(qg + qrow * D, lane, q);
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = 0.f;
-      float m = -INFINITY, l = 0.f;
-      const int nk = keys_of_query(sh, qi);
-      for (int i = 0; i < nk; ++i) {
-        float dot = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) dot += q[e] * ks[i * D + lane * E + e];
-        const float s2 = warp_sum(dot) * sh.scale_log2;
-        const float mn = fmaxf(m, s2);
-        const float c = exp2f(m - mn);
-        const float p = exp2f(s2 - mn);
-        l = l * c + p;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = acc[e] * c + p * vs[i * D + lane * E + e];
-        m = mn;
-      }
-      // Eq. 2 with the main part of the same row (its O_m and natural-log
-      // l_m are in the workspace): l = log(e^l_m + e^l_b) shifted by the
-      // larger of the two, O = e^(l_m - l) O_m + e^(l_b - l) O_b over the
-      // printed denominator; an empty part contributes nothing, whatever its
-      // O holds.  Written as the bf16 output row and the merged lse.
-      const float lb = (m + log2f(l)) * BA_LN2;
-      const float lm = a.lm[qrow];
-      const float top = fmaxf(lm, lb);
-      float res[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) res[e] = 0.f;
-      float lout = -INFINITY;
-      if (top != -INFINITY) {
-        lout = top + logf(expf(lm - top) + expf(lb - top));
-        const float wm = expf(lm - lout), wb = expf(lb - lout);
-        const float inv = 1.0f / (wm + wb);
-        if (wm > 0.f) {
-          const float* orow = a.om + qrow * D + lane * E;
-#pragma unroll
-          for (int e = 0; e < E; ++e) res[e] = wm * orow[e];
-        }
-        if (wb > 0.f) {
-          const float ib = wb / l;
-#pragma unroll
-          for (int e = 0; e < E; ++e) res[e] += ib * acc[e];
-        }
-#pragma unroll
-        for (int e = 0; e < E; ++e) res[e] *= inv;
-      }
-      store_row_bf16<D>(static_cast<__nv_bfloat16*>(a.o) + qrow * D, lane, res);
-      if (lane == 0) a.lse[qrow] = lout;
-    }
-  }
-}
-
-template <int D>
 __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
   extern __shared__ float smem[];
   constexpr int E = D / 32;
@@ -233,7 +129,6 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
   const auto* dog = static_cast<const __nv_bfloat16*>(a.d_o);
   const auto* kb = static_cast<const __nv_bfloat16*>(a.kb);
   const auto* vb = static_cast<const __nv_bfloat16*>(a.vb);
-  auto* dq = static_cast<__nv_bfloat16*>(a.dq);
   const int64_t total = sh.units * sh.Hkv;
   const int nq = rows_per_unit(sh) * sh.G;
   for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
@@ -259,10 +154,9 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
       int64_t j, r;
       unit_query(sh, u, qi, j, r);
       const int64_t qrow = (j * sh.rows + r) * sh.Hq + kvh * sh.G + g;
-      float q[E], go[E], gq[E];
+      float q[E], go[E];
       load_row<D>(qg + qrow * D, lane, q);
       load_row<D>(dog + qrow * D, lane, go);
-      load_row_f32<D>(a.dqacc + qrow * D, lane, gq);
       const int64_t srow = (j * sh.Hq + kvh * sh.G + g) * sh.rows + r;  // stream-major
       const float4 rec = a.rowrec[srow];
       const float l2 = rec.x;
@@ -284,7 +178,6 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
             const float ds = p * (dp - delta);
 #pragma unroll
             for (int e = 0; e < E; ++e) {
-              gq[e] += sh.scale * ds * ks[i * D + lane * E + e];
               dka[i][e] += sh.scale * ds * q[e];
               dva[i][e] += p * go[e];
             }
@@ -304,13 +197,11 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
           const float ds = p * (dp - delta);
 #pragma unroll
           for (int e = 0; e < E; ++e) {
-            gq[e] += sh.scale * ds * ks[i * D + lane * E + e];
             atomicAdd(&dks[i * D + lane * E + e], sh.scale * ds * q[e]);
             atomicAdd(&dvs[i * D + lane * E + e], p * go[e]);
           }
         }
       }
-      store_row_bf16<D>(dq + qrow * D, lane, gq);
     }
     if (in_regs) {
 #pragma unroll
@@ -336,23 +227,9 @@ int64_t grid_for(int64_t total) {
 
 }  // namespace
 
-cudaError_t ba_launch_branch_fwd(const BaFwdArgs& a, cudaStream_t st) {
-  const int64_t total = a.sh.units * a.sh.Hkv;
-  if (total == 0 || a.sh.nbk == 0) return cudaSuccess;
-  const size_t smem = size_t(2) * a.sh.nbk * a.sh.d * sizeof(float);
-  if (a.sh.d == 128) {
-    if (cudaError_t e = set_dynamic_smem(branch_fwd_kernel<128>, smem); e != cudaSuccess) return e;
-    branch_fwd_kernel<128><<<unsigned(grid_for(total)), 128, smem, st>>>(a);
-  } else {
-    if (cudaError_t e = set_dynamic_smem(branch_fwd_kernel<64>, smem); e != cudaSuccess) return e;
-    branch_fwd_kernel<64><<<unsigned(grid_for(total)), 128, smem, st>>>(a);
-  }
-  return cudaGetLastError();
-}
-
 cudaError_t ba_launch_branch_bwd(const BaBwdArgs& a, cudaStream_t st) {
   const int64_t total = a.sh.units * a.sh.Hkv;
-  if (total == 0) return cudaSuccess;
+  if (total == 0 || a.sh.nbk == 0) return cudaSuccess;
   const size_t smem = size_t(4) * a.sh.nbk * a.sh.d * sizeof(float);
   if (a.sh.d == 128) {
     if (cudaError_t e = set_dynamic_smem(branch_bwd_kernel<128>, smem); e != cudaSuccess) return e;

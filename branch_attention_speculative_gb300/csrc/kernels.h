@@ -12,7 +12,6 @@ struct BaFwdArgs {
   BaShape sh;
   BaTables tb;
   const void *q, *km, *vm, *kb, *vb;  // inputs (bf16)
-  float *om, *lm;                     // main partials (fp32, workspace)
   void* o;                            // output (bf16)
   float* lse;                         // lse (fp32)
   // 8-bit forward: e4m3 copies of q, k_m and V^T ([Hkv][d][T]) in the
@@ -28,7 +27,6 @@ struct BaBwdArgs {
   const void *o, *d_o;                // forward output and its gradient (bf16)
   const float* lse;                   // forward lse (fp32)
   float4* rowrec;                     // per (step, head, row), stream-major: {lse*log2e, Delta, limit, 0}
-  float* dqacc;                       // fp32 dQ accumulator, like q_b (workspace)
   void *dq, *dkm, *dvm, *dkb, *dvb;   // gradients (bf16)
   // single-step TTT calls: the key gradients are added into these fp32
   // accumulators (natural layouts) instead of being written to dkm .. dvb
@@ -44,8 +42,9 @@ inline cudaError_t set_dynamic_smem(Kernel* kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
 }
 
-// K2: causal main attention over each query tile's key segments -> O_m, l_m
-// (tcgen05 / TMEM / TMA; head_dim 64 and 128).
+// K2 (+K3, K4 in its epilogue): causal main attention over each query tile's
+// key segments, then per row the rank-local branch part and the Eq. 2 merge
+// -> o, lse (tcgen05 / TMEM / TMA; head_dim 64 and 128).
 cudaError_t ba_launch_main_fwd_tc(const BaFwdArgs& a, cudaStream_t st);
 // K2 with 8-bit operands (head_dim 128): QK^T and PV on e4m3 copies.
 cudaError_t ba_launch_main_fwd_fp8(const BaFwdArgs& a, cudaStream_t st);
@@ -53,22 +52,18 @@ cudaError_t ba_launch_main_fwd_fp8(const BaFwdArgs& a, cudaStream_t st);
 // the e4m3 copies q8, k8 and the transposed vt8 [Hkv][d][T].
 cudaError_t ba_launch_fp8_quantize(const BaFwdArgs& a, float* amax, void* q8, void* k8, void* vt8,
                                    cudaStream_t st);
-// K3 + K4: rank-local branch attention, each row merged with O_m, l_m by
-// Eq. 2 as it is computed -> o, lse.
-cudaError_t ba_launch_branch_fwd(const BaFwdArgs& a, cudaStream_t st);
-// K4 alone for plans without branch keys: O_m, l_m pass through -> o, lse.
-cudaError_t ba_launch_merge_plan(const BaFwdArgs& a, cudaStream_t st);
-// K4 on caller buffers.
+// K4 alone on caller buffers (ba_lse_merge).
 cudaError_t ba_launch_merge_rows(int64_t rows, int d, const float* om, const float* lm, const float* ob,
                                  const float* lb, void* o, float* l, cudaStream_t st);
 // K5: Delta = rowsum(dO * O) and the row records.
 cudaError_t ba_launch_bwd_prep(const BaBwdArgs& a, cudaStream_t st);
-// K6: main-attention backward on tcgen05 (head_dim 64 and 128): the
+// K6 (+K8): main-attention backward on tcgen05 (head_dim 64 and 128): the
 // key-stationary kernel writes dK_m, dV_m (natural order); the
-// query-stationary kernel writes every row of the fp32 dQ accumulator.
+// query-stationary kernel writes dq_b, adding each row's branch part in its
+// epilogue.
 cudaError_t ba_launch_main_bwd_kv_tc(const BaBwdArgs& a, cudaStream_t st);
 cudaError_t ba_launch_main_bwd_q_tc(const BaBwdArgs& a, cudaStream_t st);
-// K7 (+K8): branch backward: dK_b, dV_b (natural); dQ = accumulator + branch part -> natural bf16.
+// K7: branch backward: dK_b, dV_b (natural).
 cudaError_t ba_launch_branch_bwd(const BaBwdArgs& a, cudaStream_t st);
 
 // Self-test: a bounded wait on a barrier nothing completes (records BA_DEV_TIMEOUT).

@@ -14,9 +14,9 @@
 //              buffer it came from
 //   dQ += dS K          M=128 queries, N=d, K=128 keys; dS read from TMEM as
 //                       the A operand, K an MN-major shared operand -> TMEM
-// dQ stays in TMEM for the whole tile and is written once, scaled, into the
-// fp32 dQ accumulator (no atomics, no read-modify-write); the branch backward
-// adds the branch part and writes the bf16 result.
+// dQ stays in TMEM for the whole tile and is written once (no atomics, no
+// read-modify-write): the epilogue adds the row's branch part and writes the
+// bf16 result.
 // TMEM: S0 [0,128), S1 [128,256), dP [256,384), dQ [384,512).  Inside an S
 // buffer the warp of key half h reads fp32 columns [64h, 64h+64) and writes
 // dS (bf16 pairs) back into [64h, 64h+32): no warp writes a column another
@@ -31,13 +31,13 @@
 // head_dim 64 and 128: the kernel is templated on d (tiles of d / 64
 // 128-byte swizzled blocks; dQ takes d TMEM columns).
 // Every query row of the plan lies in exactly one tile and every tile writes
-// all of its rows (zeros for a tile without key blocks), so the accumulator
-// needs no clearing beforehand.
+// all of its rows (the main part zero for a tile without key blocks).
 #include <cudaTypedefs.h>
 #include <math.h>
 
 #include <mutex>
 
+#include "branch_row.cuh"
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -315,16 +315,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DSFULL + sb));
     }
-    // epilogue: dQ (main part, scaled) -> fp32 accumulator row, written once;
-    // each warp writes d-columns (d / 2) (w / 4) .. of its 32 rows (zeros when
-    // the tile has no key blocks)
+    // epilogue: the row's dQ is finished here.  The branch part (rainbus page,
+    // core method: local, no branch-dependent traffic) comes from the row's
+    // few branch keys: with P = exp2(s2 - lse2) from the same merged lse,
+    // dS_t = P_t (<dO, v_t> - Delta) and dq += scale * dS_t k_t.  q and dO are
+    // read from the tile's swizzled shared copies (16-byte chunk c of a row
+    // sits at chunk c ^ (row % 8)), k_t and v_t from the caller's k_b / v_b.
+    // Each warp writes d-columns (d / 2) (w / 4) .. of its 32 rows as bf16
+    // (the main part is zero when the tile has no key blocks).
     constexpr int HD = D / 2;
     const bool have = ok && i > 0 &&
                       mbar_wait_warp(bar(B_SFREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, tb.status, abort_flag);
     if (have || (ok && i == 0)) {
       if (have) tc_fence_after();
-      const int64_t qrow = (int64_t(j) * sh.rows + tile.nrow0 + r) * sh.Hq + h;
-      float4* dst = reinterpret_cast<float4*>(a.dqacc + qrow * D + half * HD);
+      const int64_t nr = tile.nrow0 + r;
+      const int64_t qrow = (int64_t(j) * sh.rows + nr) * sh.Hq + h;
+      const int nk = rok ? branch_key_count(sh, sh.step0 + j) : 0;
+      const int64_t u = branch_unit_of_row(sh, nr);
+      const auto* kbp = static_cast<const __nv_bfloat16*>(a.kb);
+      const auto* vbp = static_cast<const __nv_bfloat16*>(a.vb);
+      // dS of the branch keys (scaled by the softmax scale)
+      float dsk[BA_MAX_BRANCH_KEYS];
+      for (int t = 0; t < nk; ++t) {
+        const uint4* kp = reinterpret_cast<const uint4*>(kbp + (branch_key_row(sh, u, t) * sh.Hkv + kvh) * D);
+        const uint4* vp = reinterpret_cast<const uint4*>(vbp + (branch_key_row(sh, u, t) * sh.Hkv + kvh) * D);
+        float sdot = 0.f, pdot = 0.f;
+#pragma unroll 2
+        for (int c = 0; c < D / 8; ++c) {
+          const uint32_t off = (c >> 3) * L::TILE + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          const uint4 qv = *reinterpret_cast<const uint4*>(gbase + L::q + off);
+          const uint4 gv = *reinterpret_cast<const uint4*>(gbase + L::go + off);
+          sdot += dot8_bf16(qv, kp[c]);
+          pdot += dot8_bf16(gv, vp[c]);
+        }
+        const float p = ex2_approx(fmaf(sdot, sh.scale_log2, -l2));
+        dsk[t] = sh.scale * p * (pdot - delta);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + qrow * D + half * HD);
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         float o[32];
@@ -337,9 +364,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (rok) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[c * 8 + e] = make_float4(sh.scale * o[4 * e], sh.scale * o[4 * e + 1], sh.scale * o[4 * e + 2],
-                                         sh.scale * o[4 * e + 3]);
+          for (int e = 0; e < 32; ++e) o[e] *= sh.scale;
+          for (int t = 0; t < nk; ++t) {
+            const uint4* kp = reinterpret_cast<const uint4*>(kbp + (branch_key_row(sh, u, t) * sh.Hkv + kvh) * D +
+                                                             half * HD + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) axpy8_bf16(o + 8 * q, dsk[t], kp[q]);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[c * 4 + q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                                        pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
         }
       }
     }

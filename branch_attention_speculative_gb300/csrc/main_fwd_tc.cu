@@ -16,8 +16,10 @@
 //              diagonal chunk, keeps the row max / sum, writes P (bf16, two
 //              per 32-bit column) back into the first 64 columns of the same
 //              S buffer, rescales O in TMEM only when the row max grew by more
-//              than 2^8 (the values of P stay below 256), and finally writes
-//              O_m = O / l and l_m.
+//              than 2^8 (the values of P stay below 256), and finally
+//              finishes its row: the rank-local branch part over the row's
+//              few branch keys (read from k_b / v_b), the Eq. 2 merge with the
+//              main part O / l, and the bf16 output row and its lse.
 //   warp 4     TMA producer: Q once, then K and V blocks into three-stage rings.
 //   warp 5     owns TMEM; one thread issues S = Q K^T into one of three TMEM
 //              S buffers.
@@ -49,6 +51,7 @@
 
 #include <mutex>
 
+#include "branch_row.cuh"
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -410,13 +413,58 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL + sb));
     }
-    // epilogue: O / l and the natural-log lse of the main part
+    // epilogue: the row is finished here.  Its branch part (the few keys of
+    // its own branch, read from k_b / v_b) is computed by the row's thread,
+    // then merged with the main part O / l, l_m by Eq. 2 (rainbus page, core
+    // method): l = log(e^l_m + e^l_b) shifted by the larger of the two,
+    // O = (e^(l_m - l) O_m + e^(l_b - l) O_b) / (e^(l_m - l) + e^(l_b - l)); an
+    // empty part contributes nothing.  o (bf16) and lse are written in natural
+    // order.
     if (ok && i > 0 && mbar_wait_warp(bar(B_SFREE + (i - 1) % NSB), ((i - 1) / NSB) & 1, tb.status, abort_flag)) {
       tc_fence_after();
       const bool write = r < tile.nrows;
-      const int64_t qrow = (int64_t(j) * sh.rows + tile.nrow0 + r) * sh.Hq + h;
-      const float inv = l > 0.f ? (F8 ? f8_scale(a.f8amax[2]) : 1.f) / l : 0.f;
-      float4* dst = reinterpret_cast<float4*>(a.om + qrow * D);
+      const int64_t nr = tile.nrow0 + r;
+      const int64_t qrow = (int64_t(j) * sh.rows + nr) * sh.Hq + h;
+      const float lm = l > 0.f ? (m_used + log2f(l)) * BA_LN2 : -INFINITY;
+      // branch scores in base 2, their max and sum (online)
+      const int nk = write ? branch_key_count(sh, sh.step0 + j) : 0;
+      const int64_t u = branch_unit_of_row(sh, nr);
+      const auto* kbp = static_cast<const __nv_bfloat16*>(a.kb);
+      const auto* vbp = static_cast<const __nv_bfloat16*>(a.vb);
+      float sc[BA_MAX_BRANCH_KEYS];
+      float mb = -INFINITY, lsb = 0.f;
+      if (nk > 0) {
+        uint4 qv[D / 8];
+        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + qrow * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) qv[c] = qp[c];
+        for (int t = 0; t < nk; ++t) {
+          const uint4* kp = reinterpret_cast<const uint4*>(kbp + (branch_key_row(sh, u, t) * sh.Hkv + kvh) * D);
+          float dot = 0.f;
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) dot += dot8_bf16(qv[c], kp[c]);
+          const float s2 = dot * sh.scale_log2;
+          sc[t] = s2;
+          const float mn = fmaxf(mb, s2);
+          lsb = lsb * ex2_approx(mb - mn) + ex2_approx(s2 - mn);
+          mb = mn;
+        }
+      }
+      const float lb = nk > 0 ? (mb + log2f(lsb)) * BA_LN2 : -INFINITY;
+      const float top = fmaxf(lm, lb);
+      float wm = 0.f, wb = 0.f, lout = -INFINITY;
+      if (top != -INFINITY) {
+        lout = top + logf(expf(lm - top) + expf(lb - top));
+        wm = expf(lm - lout);
+        wb = expf(lb - lout);
+        const float den = 1.0f / (wm + wb);
+        wm *= den;
+        wb *= den;
+      }
+      // O_m = O (TMEM) * s_v / l; O_b = sum_t p_t v_t / sum_t p_t
+      const float cm = l > 0.f ? wm * (F8 ? f8_scale(a.f8amax[2]) : 1.f) / l : 0.f;
+      const float cb = nk > 0 ? wb / lsb : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + qrow * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
@@ -424,11 +472,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_wait_ld();
         if (write) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[c * 8 + e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+          for (int e = 0; e < 32; ++e) o[e] = wm > 0.f ? cm * o[e] : 0.f;
+          if (wb > 0.f) {
+            for (int t = 0; t < nk; ++t) {
+              const float p = ex2_approx(sc[t] - mb) * cb;
+              const uint4* vp =
+                  reinterpret_cast<const uint4*>(vbp + (branch_key_row(sh, u, t) * sh.Hkv + kvh) * D + c * 32);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) axpy8_bf16(o + 8 * q, p, vp[q]);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[c * 4 + q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                                        pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
         }
       }
-      if (write) a.lm[qrow] = l > 0.f ? (m_used + log2f(l)) * BA_LN2 : -INFINITY;
+      if (write) a.lse[qrow] = lout;
     }
   }
   tc_fence_before();

@@ -68,12 +68,3 @@ cudaError_t ba_launch_merge_rows(int64_t rows, int d, const float* om, const flo
     lse_merge_kernel<64><<<unsigned(blocks), 256, 0, st>>>(rows, om, lm, ob, lb, o16, l);
   return cudaGetLastError();
 }
-
-// The plan's merge pass over every (step, row, head) of the query space, used
-// when the plan has no branch keys (the CAUSAL family): the main partial
-// passes through (O_b absent, l_b = -inf).  With branch keys the branch
-// kernel merges each row itself.
-cudaError_t ba_launch_merge_plan(const BaFwdArgs& a, cudaStream_t st) {
-  const int64_t rows = int64_t(a.sh.steps) * a.sh.rows * a.sh.Hq;
-  return ba_launch_merge_rows(rows, a.sh.d, a.om, a.lm, nullptr, nullptr, a.o, a.lse, st);
-}

@@ -353,18 +353,12 @@ int ba_build_plan(const ba_plan_desc* d, ba_plan* p) {
   off += t;
   const size_t qrows = size_t(sh.steps) * size_t(rows) * size_t(sh.Hq);
   const size_t dd = size_t(sh.d);
-  // The kernels read the caller's natural-layout tensors directly, so the
-  // workspace holds only partials: forward O_m, l_m (the branch kernel merges
-  // its part into the output row by row), backward row records and the fp32
-  // dQ accumulator.  The two regions overlap.
-  const size_t scratch = off;
-  size_t f = scratch;
-  w.om = f; f = align256(f + qrows * dd * 4);
-  w.lm = f; f = align256(f + qrows * 4);
-  size_t b = scratch;
-  w.rowrec = b; b = align256(b + qrows * 16);
-  w.dqacc = b; b = align256(b + qrows * dd * 4);
-  w.total = std::max(f, b);
+  // The kernels read the caller's natural-layout tensors directly and finish
+  // every output row in their epilogues, so the workspace holds only the
+  // backward's row records.
+  w.rowrec = off;
+  off = align256(off + qrows * 16);
+  w.total = off;
   size_t g = align256(w.total);
   w.f8_amax = g; g += 256;
   w.f8_q = g; g = align256(g + qrows * dd);

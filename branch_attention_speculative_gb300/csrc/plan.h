@@ -15,8 +15,7 @@ struct BaWorkspaceLayout {
   size_t tables;                  // start of the uploaded table image
   size_t table_bytes;             // size of the table image
   size_t t_row_lim, t_nat_lim, t_tok_perm, t_anc_perm, t_fq, t_fseg, t_forder, t_bq, t_bkv, t_bqr, t_border;
-  size_t om, lm;                  // forward main partials (fp32, natural order)
-  size_t rowrec, dqacc;           // backward scratch: row records (16 B), dQ (fp32), natural order
+  size_t rowrec;                  // backward scratch: row records (16 B), natural order
   size_t total;
   // 8-bit forward (after `total`, so it overlaps neither scratch region):
   // amax[3], e4m3 copies of q and k_m, the transposed e4m3 V^T [Hkv][d][T]

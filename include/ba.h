@@ -166,8 +166,9 @@ size_t ba_workspace_bytes(ba_plan_t plan);
  * attention for each query tile over its key chunks in ring order, with the
  * online-softmax merge between ring steps; the zigzag layout lives only in the
  * plan's tile tables, so q_b, k_m and v_m are read in place (no packed
- * copies).  Then rank-local branch attention, fused with the Eq. 2 merge of
- * each row's two parts, writes o and lse in natural order.
+ * copies).  Each row then gets its rank-local branch part and the Eq. 2 merge
+ * of the two parts in the same kernel, which writes o and lse in natural
+ * order.
  * Inputs q_b, k_m, v_m, k_b, v_b; outputs o (bf16) and lse (fp32). */
 int ba_forward(ba_plan_t plan, const void* q_b, const void* k_m, const void* v_m,
                const void* k_b, const void* v_b, void* o, float* lse,
@@ -307,8 +308,8 @@ int ba_lse_merge(int64_t rows, int32_t head_dim, const float* o_m, const float* 
  * and reused; no device memory is allocated).  ba_profile_read waits for the
  * recorded events, adds their elapsed times per kernel name since the last
  * read, writes up to `capacity` entries and returns the entry count in
- * *count.  Names: zigzag_pack, main_fwd, branch_fwd, lse_merge, bwd_prep,
- * main_bwd_kv, main_bwd_dq, branch_bwd, fp8_quantize, main_fwd_fp8. */
+ * *count.  Names: zigzag_pack, main_fwd, bwd_prep, main_bwd_kv, main_bwd_dq,
+ * branch_bwd, fp8_quantize, main_fwd_fp8. */
 typedef struct {
   char name[24];
   int64_t launches;
