@@ -337,7 +337,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // max-first path gives.  Otherwise (a row's first keys, or a rare grow)
       // the scores are reloaded and the block is done max-first.
       bool fast = __all_sync(0xffffffffu, m_used != -INFINITY);
-      if (fast) {
+      if (F8 && fast) {
+        // 8-bit path: P is stored as e4m3 (3 mantissa bits), so it is computed
+        // in packed halves — two exponents per fp32x2 FMA, one f16x2 ex2 and
+        // one e4m3x2 conversion per pair, and an f16x2 tree for the block's
+        // row sum (relative error below 2^-8, against e4m3's 2^-4).  A grown
+        // max shows as a sum above 2^8 (or an f16 overflow to inf) and takes
+        // the fp32 max-first path below.
+        const float2 sc2 = make_float2(sl2, sl2), mm2 = make_float2(-m_used, -m_used);
+        __half2 h[TBN / 2];
+#pragma unroll
+        for (int c = 0; c < TBN / 2; ++c) {
+          const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sc2, mm2);
+          h[c] = h2exp2(__floats2half2_rn(x.x, x.y));
+        }
+        __half2 t[TBN / 4];
+#pragma unroll
+        for (int c = 0; c < TBN / 4; ++c) t[c] = __hadd2(h[2 * c], h[2 * c + 1]);
+#pragma unroll
+        for (int w = TBN / 8; w >= 1; w >>= 1) {
+#pragma unroll
+          for (int c = 0; c < w; ++c) t[c] = __hadd2(t[c], t[c + w]);
+        }
+        const float2 tf = __half22float2(t[0]);
+        const float rs = tf.x + tf.y;
+        if (__any_sync(0xffffffffu, !(rs <= 256.f))) {
+          fast = false;
+        } else {
+          l += rs;
+#pragma unroll
+          for (int g = 0; g < TBN / 32; ++g) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t lo = __nv_cvt_halfraw2_to_fp8x2(__half2_raw(h[16 * g + 2 * e]), __NV_SATFINITE, __NV_E4M3);
+              const uint32_t hi =
+                  __nv_cvt_halfraw2_to_fp8x2(__half2_raw(h[16 * g + 2 * e + 1]), __NV_SATFINITE, __NV_E4M3);
+              w[e] = lo | (hi << 16);
+            }
+            tmem_st8(tS + lane_off + sb * TBN + g * 8, w);
+          }
+        }
+      } else if (fast) {
         float rsp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < TBN; ++c) {
@@ -461,32 +502,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         wm *= den;
         wb *= den;
       }
-      // O_m = O (TMEM) * s_v / l; O_b = sum_t p_t v_t / sum_t p_t
+      // O_m = O (TMEM) * s_v / l; O_b = sum_t p_t v_t / sum_t p_t.  The whole
+      // row sits in registers while the branch values are added key by key,
+      // so each key costs one round of 16-byte loads of its v row.
       const float cm = l > 0.f ? wm * (F8 ? f8_scale(a.f8amax[2]) : 1.f) / l : 0.f;
       const float cb = nk > 0 ? wb / lsb : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + qrow * D);
+      float o[D];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
-        tmem_wait_ld();
-        if (write) {
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + lane_off + c * 32, o + 32 * c);
+      tmem_wait_ld();
+      if (write) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = wm > 0.f ? cm * o[e] : 0.f;
-          if (wb > 0.f) {
-            for (int t = 0; t < nk; ++t) {
-              const float p = ex2_approx(sc[t] - mb) * cb;
-              const uint4* vp =
-                  reinterpret_cast<const uint4*>(vbp + (branch_key_row(sh, u, t) * sh.Hkv + kvh) * D + c * 32);
+        for (int e = 0; e < D; ++e) o[e] = wm > 0.f ? cm * o[e] : 0.f;
+        if (wb > 0.f) {
+          for (int t = 0; t < nk; ++t) {
+            const float p = ex2_approx(sc[t] - mb) * cb;
+            const uint4* vp = reinterpret_cast<const uint4*>(vbp + (branch_key_row(sh, u, t) * sh.Hkv + kvh) * D);
+            uint4 vv[D / 8];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) axpy8_bf16(o + 8 * q, p, vp[q]);
-            }
+            for (int q = 0; q < D / 8; ++q) vv[q] = vp[q];
+#pragma unroll
+            for (int q = 0; q < D / 8; ++q) axpy8_bf16(o + 8 * q, p, vv[q]);
           }
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[c * 4 + q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
-                                        pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
         }
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + qrow * D);
+#pragma unroll
+        for (int q = 0; q < D / 8; ++q)
+          dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                              pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
       }
       if (write) a.lse[qrow] = lout;
     }
