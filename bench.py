@@ -239,8 +239,8 @@ def kernel_bytes(wl, info, name):
         return R * (2 * d * 4 + 2 * 4) + R * (d * 2 + 4)
     if name == "bwd_prep":  # read o, dO, lse; write the row record
         return R * (2 * d * 2 + 4) + R * 16
-    if name == "branch_bwd":  # read q, dO, the row records, k_b, v_b; write dk_b, dv_b
-        return R * (2 * d * 2 + 16) + 2 * nbk * d * 2 + 2 * nbk * d * 2
+    if name == "branch_bwd":  # read q, dO, dq (main part), the row records, k_b, v_b; write dq, dk_b, dv_b
+        return R * (3 * d * 2 + 16) + 2 * nbk * d * 2 + R * d * 2 + 2 * nbk * d * 2
     return None
 
 

@@ -11,7 +11,7 @@
 #define BA_FWD_BN 64    // keys per forward key block (work estimate only)
 #define BA_BWD_BM 64    // query rows per backward query tile
 #define BA_BWD_BN 128   // keys per backward key tile
-#define BA_BWD_CS 4     // key tiles per thread-block cluster of the dK/dV kernel:
+#define BA_BWD_CS 2     // key tiles per thread-block cluster of the dK/dV kernel:
                         // the tiles of a cluster come from one chunk and meet
                         // the same query tiles in the same order; the cluster
                         // only makes them run side by side, so each CTA's own

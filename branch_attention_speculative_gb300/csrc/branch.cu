@@ -16,10 +16,10 @@
 // its rows (every step and q head of the group) before one store.  The work is
 // tiny next to the main part and bound by HBM traffic of q and dO.
 //
-// The forward's branch part and Eq. 2 merge, and the branch part of dQ, are
-// computed per row in the epilogues of the main-attention kernels, which own
-// those rows; only the key gradients, which sum over rows of many CTAs there,
-// are gathered here.
+// It also finishes dQ: the main part arrives as bf16 in dq_b (written by the
+// dQ kernel), the branch part is added in fp32 and the row is written back.
+// The forward's branch part and Eq. 2 merge run in the main forward's
+// epilogue instead, where each row's thread already holds its main part.
 #include <math.h>
 
 #include "device.cuh"
@@ -60,6 +60,19 @@ __device__ __forceinline__ void load_row(const __nv_bfloat16* p, int lane, float
   } else {
     const float2 a = unpack_bf16(reinterpret_cast<const uint32_t*>(p)[lane]);
     x[0] = a.x; x[1] = a.y;
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* p, int lane, const float* x) {
+  constexpr int E = D / 32;
+  if constexpr (E == 4) {
+    uint2 v;
+    v.x = pack_bf16(x[0], x[1]);
+    v.y = pack_bf16(x[2], x[3]);
+    reinterpret_cast<uint2*>(p)[lane] = v;
+  } else {
+    reinterpret_cast<uint32_t*>(p)[lane] = pack_bf16(x[0], x[1]);
   }
 }
 
@@ -129,6 +142,7 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
   const auto* dog = static_cast<const __nv_bfloat16*>(a.d_o);
   const auto* kb = static_cast<const __nv_bfloat16*>(a.kb);
   const auto* vb = static_cast<const __nv_bfloat16*>(a.vb);
+  auto* dq = static_cast<__nv_bfloat16*>(a.dq);
   const int64_t total = sh.units * sh.Hkv;
   const int nq = rows_per_unit(sh) * sh.G;
   for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
@@ -154,9 +168,10 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
       int64_t j, r;
       unit_query(sh, u, qi, j, r);
       const int64_t qrow = (j * sh.rows + r) * sh.Hq + kvh * sh.G + g;
-      float q[E], go[E];
+      float q[E], go[E], gq[E];
       load_row<D>(qg + qrow * D, lane, q);
       load_row<D>(dog + qrow * D, lane, go);
+      load_row<D>(dq + qrow * D, lane, gq);
       const int64_t srow = (j * sh.Hq + kvh * sh.G + g) * sh.rows + r;  // stream-major
       const float4 rec = a.rowrec[srow];
       const float l2 = rec.x;
@@ -178,6 +193,7 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
             const float ds = p * (dp - delta);
 #pragma unroll
             for (int e = 0; e < E; ++e) {
+              gq[e] += sh.scale * ds * ks[i * D + lane * E + e];
               dka[i][e] += sh.scale * ds * q[e];
               dva[i][e] += p * go[e];
             }
@@ -197,11 +213,13 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
           const float ds = p * (dp - delta);
 #pragma unroll
           for (int e = 0; e < E; ++e) {
+            gq[e] += sh.scale * ds * ks[i * D + lane * E + e];
             atomicAdd(&dks[i * D + lane * E + e], sh.scale * ds * q[e]);
             atomicAdd(&dvs[i * D + lane * E + e], p * go[e]);
           }
         }
       }
+      store_row_bf16<D>(dq + qrow * D, lane, gq);
     }
     if (in_regs) {
 #pragma unroll

@@ -57,13 +57,13 @@ cudaError_t ba_launch_merge_rows(int64_t rows, int d, const float* om, const flo
                                  const float* lb, void* o, float* l, cudaStream_t st);
 // K5: Delta = rowsum(dO * O) and the row records.
 cudaError_t ba_launch_bwd_prep(const BaBwdArgs& a, cudaStream_t st);
-// K6 (+K8): main-attention backward on tcgen05 (head_dim 64 and 128): the
+// K6: main-attention backward on tcgen05 (head_dim 64 and 128): the
 // key-stationary kernel writes dK_m, dV_m (natural order); the
-// query-stationary kernel writes dq_b, adding each row's branch part in its
-// epilogue.
+// query-stationary kernel writes the main part of dq_b (bf16).
 cudaError_t ba_launch_main_bwd_kv_tc(const BaBwdArgs& a, cudaStream_t st);
 cudaError_t ba_launch_main_bwd_q_tc(const BaBwdArgs& a, cudaStream_t st);
-// K7: branch backward: dK_b, dV_b (natural).
+// K7 (+K8): branch backward: dK_b, dV_b (natural); adds each row's branch
+// part to dq_b.
 cudaError_t ba_launch_branch_bwd(const BaBwdArgs& a, cudaStream_t st);
 
 // Self-test: a bounded wait on a barrier nothing completes (records BA_DEV_TIMEOUT).

@@ -15,8 +15,8 @@
 //   dQ += dS K          M=128 queries, N=d, K=128 keys; dS read from TMEM as
 //                       the A operand, K an MN-major shared operand -> TMEM
 // dQ stays in TMEM for the whole tile and is written once (no atomics, no
-// read-modify-write): the epilogue adds the row's branch part and writes the
-// bf16 result.
+// read-modify-write) as bf16 into dq_b; the branch kernel, which stages each
+// anchor's branch keys once for all of its rows, adds the branch part.
 // TMEM: S0 [0,128), S1 [128,256), dP [256,384), dQ [384,512).  Inside an S
 // buffer the warp of key half h reads fp32 columns [64h, 64h+64) and writes
 // dS (bf16 pairs) back into [64h, 64h+32): no warp writes a column another
@@ -37,7 +37,6 @@
 
 #include <mutex>
 
-#include "branch_row.cuh"
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -315,82 +314,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DSFULL + sb));
     }
-    // epilogue: the row's dQ is finished here.  The branch part (rainbus page,
-    // core method: local, no branch-dependent traffic) comes from the row's
-    // few branch keys: with P = exp2(s2 - lse2) from the same merged lse,
-    // dS_t = P_t (<dO, v_t> - Delta) and dq += scale * dS_t k_t.  Each of the
-    // row's two threads (warps w and w + 4) works on its half of the d
-    // columns: it forms partial dot products of q and dO (read from the
-    // tile's swizzled shared copies: 16-byte chunk c of a row sits at chunk
-    // c ^ (row % 8)) with its halves of k_t and v_t (from the caller's k_b /
-    // v_b), the two halves meet in shared memory (the K ring, idle once the
-    // last GEMM has finished), and each thread adds scale * dS_t k_t to its
-    // columns and writes them as bf16.  Keys go in batches of 16, so the
-    // partials take 32 KB whatever the block size.
+    // epilogue: dQ (main part, scaled) -> bf16 dq row, written once; each warp
+    // writes d-columns (d / 2) (w / 4) .. of its 32 rows (zeros when the tile
+    // has no key blocks).  The branch kernel adds each row's branch part.
     constexpr int HD = D / 2;
-    constexpr int KBATCH = 16;
     const bool have = ok && i > 0 &&
                       mbar_wait_warp(bar(B_SFREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, tb.status, abort_flag);
-    const bool live = have || (ok && i == 0);
-    if (have) tc_fence_after();
-    // the main part, scaled (zero when the tile had no key blocks)
-    float o[HD];
-    if (have) {
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c) tmem_ld32(tDQ + lane_off + half * HD + c * 32, o + 32 * c);
-      tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < HD; ++e) o[e] *= sh.scale;
-    } else {
-#pragma unroll
-      for (int e = 0; e < HD; ++e) o[e] = 0.f;
-    }
-    const bool act = live && rok;
-    const int nk = branch_key_count(sh, sh.step0 + j);  // the same for every row of the tile
-    const int64_t nr = tile.nrow0 + r;
-    const int64_t u = branch_unit_of_row(sh, nr);
-    const auto* kbp = static_cast<const __nv_bfloat16*>(a.kb);
-    const auto* vbp = static_cast<const __nv_bfloat16*>(a.vb);
-    float2* part = reinterpret_cast<float2*>(gbase + L::k);  // [KBATCH][128 rows][2 halves]
-    for (int t0 = 0; t0 < nk; t0 += KBATCH) {
-      const int tn = min(KBATCH, nk - t0);
-      if (act) {
-        for (int tt = 0; tt < tn; ++tt) {
-          const int64_t kr = (branch_key_row(sh, u, t0 + tt) * sh.Hkv + kvh) * D + half * HD;
-          const uint4* kp = reinterpret_cast<const uint4*>(kbp + kr);
-          const uint4* vp = reinterpret_cast<const uint4*>(vbp + kr);
-          float sd = 0.f, pd = 0.f;
-#pragma unroll
-          for (int c = 0; c < HD / 8; ++c) {
-            const int cc = half * (HD / 8) + c;  // 16-byte chunk of the whole row
-            const uint32_t off = (cc >> 3) * L::TILE + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
-            sd += dot8_bf16(*reinterpret_cast<const uint4*>(gbase + L::q + off), kp[c]);
-            pd += dot8_bf16(*reinterpret_cast<const uint4*>(gbase + L::go + off), vp[c]);
-          }
-          part[(tt * 128 + r) * 2 + half] = make_float2(sd, pd);
-        }
-      }
-      named_bar_sync(1, 256);  // the 8 compute warps
-      if (act) {
-        for (int tt = 0; tt < tn; ++tt) {
-          const float2 x = part[(tt * 128 + r) * 2], y = part[(tt * 128 + r) * 2 + 1];
-          const float p = ex2_approx(fmaf(x.x + y.x, sh.scale_log2, -l2));
-          const float ds = sh.scale * p * ((x.y + y.y) - delta);
-          const uint4* kp =
-              reinterpret_cast<const uint4*>(kbp + (branch_key_row(sh, u, t0 + tt) * sh.Hkv + kvh) * D + half * HD);
-#pragma unroll
-          for (int c = 0; c < HD / 8; ++c) axpy8_bf16(o + 8 * c, ds, kp[c]);
-        }
-      }
-      named_bar_sync(1, 256);  // the next batch reuses the partials' space
-    }
-    if (act) {
-      const int64_t qrow = (int64_t(j) * sh.rows + nr) * sh.Hq + h;
+    if (have || (ok && i == 0)) {
+      if (have) tc_fence_after();
+      const int64_t qrow = (int64_t(j) * sh.rows + tile.nrow0 + r) * sh.Hq + h;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + qrow * D + half * HD);
 #pragma unroll
-      for (int c = 0; c < HD / 8; ++c)
-        dst[c] = make_uint4(pack_bf16(o[8 * c], o[8 * c + 1]), pack_bf16(o[8 * c + 2], o[8 * c + 3]),
-                            pack_bf16(o[8 * c + 4], o[8 * c + 5]), pack_bf16(o[8 * c + 6], o[8 * c + 7]));
+      for (int c = 0; c < HD / 32; ++c) {
+        float o[32];
+        if (have) {
+          tmem_ld32(tDQ + lane_off + half * HD + c * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        if (rok) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[c * 4 + q] = make_uint4(
+                pack_bf16(sh.scale * o[8 * q], sh.scale * o[8 * q + 1]),
+                pack_bf16(sh.scale * o[8 * q + 2], sh.scale * o[8 * q + 3]),
+                pack_bf16(sh.scale * o[8 * q + 4], sh.scale * o[8 * q + 5]),
+                pack_bf16(sh.scale * o[8 * q + 6], sh.scale * o[8 * q + 7]));
+        }
+      }
     }
   }
   tc_fence_before();

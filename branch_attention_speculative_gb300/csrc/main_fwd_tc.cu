@@ -136,6 +136,29 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return lo | (hi << 16);
 }
 
+// (a0 * b + c, a1 * b + c) in one packed fp32x2 FMA, rounded to f16x2
+// (a0 in the low half).
+__device__ __forceinline__ uint32_t fma_f32x2(float a0, float a1, float b, float c) {
+  uint32_t h;
+  asm("{\n .reg .b64 a, bb, cc, d;\n .reg .f32 d0, d1;\n"
+      " mov.b64 a, {%1, %2};\n mov.b64 bb, {%3, %3};\n mov.b64 cc, {%4, %4};\n"
+      " fma.rn.f32x2 d, a, bb, cc;\n mov.b64 {d0, d1}, d;\n"
+      " cvt.rn.f16x2.f32 %0, d1, d0;\n}\n"
+      : "=r"(h)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+  return h;
+}
+
+// 2^x for both halves of an f16x2 (one MUFU instruction for the pair).
+__device__ __forceinline__ __half2 ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;\n" : "=r"(y) : "r"(x));
+  __half2_raw r;
+  r.x = static_cast<unsigned short>(y & 0xffffu);
+  r.y = static_cast<unsigned short>(y >> 16);
+  return __half2(r);
+}
+
 // Per-tensor fp8 scale from an amax (amax / 448, or 1 for an all-zero tensor).
 __device__ __forceinline__ float f8_scale(float amax) { return amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f; }
 
@@ -344,13 +367,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // row sum (relative error below 2^-8, against e4m3's 2^-4).  A grown
         // max shows as a sum above 2^8 (or an f16 overflow to inf) and takes
         // the fp32 max-first path below.
-        const float2 sc2 = make_float2(sl2, sl2), mm2 = make_float2(-m_used, -m_used);
         __half2 h[TBN / 2];
 #pragma unroll
-        for (int c = 0; c < TBN / 2; ++c) {
-          const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), sc2, mm2);
-          h[c] = h2exp2(__floats2half2_rn(x.x, x.y));
-        }
+        for (int c = 0; c < TBN / 2; ++c)
+          h[c] = ex2_f16x2(fma_f32x2(s[2 * c], s[2 * c + 1], sl2, -m_used));
         __half2 t[TBN / 4];
 #pragma unroll
         for (int c = 0; c < TBN / 4; ++c) t[c] = __hadd2(h[2 * c], h[2 * c + 1]);

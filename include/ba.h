@@ -121,7 +121,7 @@ typedef enum {
                                 limit when diag = 1                             */
   BA_TABLE_BWD_QTILES = 6,   /* [n][10] backward query tiles, fields as FWD_QTILES */
   BA_TABLE_BWD_KVTILES = 7,  /* [n][8] backward key tiles: {k0, nkeys, pos0, qr0,
-                                nqr, work, chunk, 0}, in groups of four tiles of
+                                nqr, work, chunk, 0}, in groups of two tiles of
                                 one chunk that share their query ranges (one
                                 thread-block cluster); nkeys = 0 for the fillers
                                 that complete a group                           */

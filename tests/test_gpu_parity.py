@@ -139,6 +139,11 @@ SMALL = [
             name="ttt_d128_tiles_c2"),
     W.small("block", [1536, 512], heads_q=8, heads_kv=2, head_dim=128, cp=2, block=16, anchors_per_seq=40, seed=8,
             name="block16_d128_tiles_c2"),
+    # the planner's limits on branch keys per query: block size 64, TTT depth 16
+    W.small("block", [512, 256], heads_q=4, heads_kv=2, head_dim=64, cp=2, block=64, anchors_per_seq=5, seed=10,
+            name="block64_c2"),
+    W.small("ttt", [128, 64], heads_q=2, heads_kv=1, head_dim=128, cp=2, depth=16, seed=11, name="ttt_depth16"),
+    W.small("causal", [384, 640], heads_q=4, heads_kv=2, head_dim=128, cp=2, seed=9, name="causal_d128_gqa"),
 ]
 
 
@@ -156,7 +161,7 @@ def test_config1_full_parity(api):
 
 # Main-key gradient windows at the end of the last sequence: at the 256K shape
 # one whole 128-key tile, whose attending query rows sit more than 2^31
-# elements into q_b; at the 128K block shape four tiles, one cluster of the
+# elements into q_b; at the 128K block shape four tiles, two clusters of the
 # dK/dV kernel.
 @pytest.mark.parametrize("k,n_units,window", [(2, 48, 64), (3, 32, 256), (4, 24, 512), (5, 24, 128)])
 def test_config_sampled_parity(api, k, n_units, window):
