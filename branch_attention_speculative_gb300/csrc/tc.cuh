@@ -110,15 +110,6 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   return v;
 }
 
-// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32) of the CTA.
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-
 // ---------------------------------------------------------------- TMEM
 
 // Warp-wide: allocates `ncols` TMEM columns, writes the base address to smem.

@@ -91,8 +91,11 @@ def test_fp8_forward_sampled(api, k, n_units):
     _check(og, np.concatenate([e["o"] for e in res]), lg, np.concatenate([e["lse"] for e in res]), wl.name)
 
 
-def test_fp8_rejects_unaligned_chunks(api):
-    wl = W.small("ttt", [200, 56], heads_q=2, heads_kv=1, head_dim=128, cp=2, depth=2)  # chunks of 50 and 14
+@pytest.mark.parametrize("wl", [
+    W.small("ttt", [200, 56], heads_q=2, heads_kv=1, head_dim=128, cp=2, depth=2),  # chunks of 50 and 14 tokens
+    W.small("ttt", [256], heads_q=2, heads_kv=1, head_dim=64, cp=2, depth=2),       # head_dim 64
+], ids=["unaligned_chunks", "head_dim_64"])
+def test_fp8_rejects_what_it_does_not_cover(api, wl):
     plan = api.Plan.from_workload(wl)
     t = W.make_tensors(wl, device="cuda", gen_device="cpu")
     with pytest.raises(api.BaError) as e:
