@@ -9,7 +9,7 @@
 // and main keys of every zigzag chunk into tiles of these sizes.
 #define BA_FWD_BM 128   // query rows per forward tile
 #define BA_FWD_BN 64    // keys per forward key block (work estimate only)
-#define BA_BWD_BM 64    // query rows per backward query tile
+#define BA_BWD_BM 128   // query rows per backward query tile
 #define BA_BWD_BN 128   // keys per backward key tile
 #define BA_BWD_CS 2     // key tiles per thread-block cluster of the dK/dV kernel:
                         // the tiles of a cluster come from one chunk and meet

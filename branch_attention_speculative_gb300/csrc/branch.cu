@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(128) branch_bwd_kernel(BaBwdArgs a) {
       load_row<D>(dq + qrow * D, lane, gq);
       const int64_t srow = (j * sh.Hq + kvh * sh.G + g) * sh.rows + r;  // stream-major
       const float4 rec = a.rowrec[srow];
-      const float l2 = rec.x;
+      const float l2 = -rec.x;  // lse * log2e
       const float delta = rec.y;
       const int nk = keys_of_query(sh, qi);
       if (in_regs) {

@@ -26,7 +26,7 @@ struct BaBwdArgs {
   const void *q, *km, *vm, *kb, *vb;  // inputs (bf16)
   const void *o, *d_o;                // forward output and its gradient (bf16)
   const float* lse;                   // forward lse (fp32)
-  float4* rowrec;                     // per (step, head, row), stream-major: {lse*log2e, Delta, limit, 0}
+  float4* rowrec;                     // per (step, head, row), stream-major: {-lse*log2e, Delta, limit, 0}
   void *dq, *dkm, *dvm, *dkb, *dvb;   // gradients (bf16)
   // single-step TTT calls: the key gradients are added into these fp32
   // accumulators (natural layouts) instead of being written to dkm .. dvb

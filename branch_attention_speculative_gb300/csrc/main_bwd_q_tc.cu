@@ -257,11 +257,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const bool rok = r < tile.nrows;
-    float l2 = 0.f, delta = 0.f;
+    float nl2 = 0.f, delta = 0.f;  // -lse*log2e, Delta
     int lim = -1;
     if (rok) {
       const float4 rec = a.rowrec[(int64_t(j) * sh.Hq + h) * sh.rows + tile.nrow0 + r];
-      l2 = rec.x;
+      nl2 = rec.x;
       delta = rec.y;
       lim = __float_as_int(rec.z);
     }
@@ -295,12 +295,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (climit >= KBN) {  // full block (the common case): no mask
 #pragma unroll
           for (int e = 32 * g; e < 32 * g + 32; ++e)
-            s[e] = ex2_approx(fmaf(s[e], sh.scale_log2, -l2)) * (dp[e] - delta);
+            s[e] = ex2_approx(fmaf(s[e], sh.scale_log2, nl2)) * (dp[e] - delta);
         } else {
 #pragma unroll
           for (int e = 32 * g; e < 32 * g + 32; ++e) {
             const int c = half * 64 + e;
-            const float p = ex2_approx(fmaf(s[e], sh.scale_log2, -l2));
+            const float p = ex2_approx(fmaf(s[e], sh.scale_log2, nl2));
             s[e] = (c < climit ? p : 0.f) * (dp[e] - delta);
           }
         }

@@ -9,42 +9,41 @@
 // of its group.  P is recomputed from the merged lse (exact for both key sets,
 // because Eq. 2's merged result is the single softmax over their union).
 //
-// Per (query tile, key tile) pair, on the tensor cores:
-//   S^T  = K Q^T        M=128 keys, N=64 queries, K=d; K read from TMEM  -> TMEM S^T buffer
-//   dP^T = V dO^T       same, V a shared-memory operand                   -> TMEM dP^T buffer
-//   (threads)  P^T = exp2(S^T * scale*log2e - lse*log2e),  dS^T = P^T (dP^T - Delta)
-//              written as bf16 into the P/dS buffer
-//   dV  += P^T dO       M=128 keys, N=d, K=64 queries; P^T read from TMEM,
+// Per (query tile, key tile) pair, on the tensor cores (tiles of 128 queries,
+// so every GEMM has N = 128):
+//   S^T  = K Q^T        M=128 keys, N=128 queries, K=d        -> TMEM S^T buffer
+//   dP^T = V dO^T       same                                  -> TMEM dP^T buffer
+//   (threads)  P^T = exp2(S^T * scale*log2e - lse*log2e),  dS^T = P^T (dP^T - Delta),
+//              in packed bf16x2 arithmetic, written over the buffer each came from
+//   dV  += P^T dO       M=128 keys, N=d, K=128 queries; P^T read from TMEM,
 //                       dO an MN-major shared operand
 //   dK  += dS^T Q       same, dS^T from TMEM
 // dK and dV stay in TMEM for the whole CTA and are written once, in natural
 // order, at the end.  dQ is computed by the query-stationary kernel
 // (main_bwd_q_tc.cu), which needs no atomics.
-// Shared-memory bandwidth, not the tensor pipe, bounds this shape: an N=64
-// GEMM with both operands in shared memory reads 6 KB per 32-cycle MMA, more
-// than the 128 bytes per clock shared memory delivers.  The key tile is
-// stationary, so the threads copy K into TMEM once and the S^T GEMM reads only
-// its Q operand from shared memory.
-// TMEM columns: K (bf16 pairs) [0,64), S^T [64,128), dP^T [128,192), P/dS
-// [192,256), dK [256,384), dV [384,512).  The S^T and dP^T buffers are free
-// again as soon as the threads have loaded them, so the next pair's S^T and
-// dP^T GEMMs run while the threads work on this one.  The P/dS buffer is busy
-// from the threads' P^T store until the pair's dK GEMM has read it; the
-// threads compute the next pair's P^T in registers meanwhile.  The threads
-// store P^T first and signal it, so the dV GEMM runs while they compute dS^T;
-// the dK GEMM follows dS^T.  Inside the P/dS buffer the warp of query half h
-// (queries 32h..32h+31) writes P^T (bf16 pairs) at [32h, 32h+16) and dS^T at
-// [32h+16, 32h+32).
+// Why 128 queries: one tcgen05.mma costs at least about 46 cycles whatever its
+// N (about 55 with A in TMEM), so an N=64 MMA (32 cycles of tensor work) runs
+// the tensor pipe at two thirds of its rate, while an N=128 one (64 cycles)
+// runs it at the full rate.  The price is TMEM: S^T, dP^T, dK and dV take
+// 128 columns each, so P^T and dS^T are written over the S^T and dP^T values
+// they came from, and K stays in shared memory.
+// TMEM columns: S^T / P^T [0,128), dP^T / dS^T [128,256), dK [256,256+d), dV
+// after it.  Inside the S^T buffer the warp of query half h (queries
+// 64h..64h+63) reads fp32 columns [64h, 64h+64) and writes P^T (bf16 pairs)
+// into [64h, 64h+32), so no warp writes a column another warp still has to
+// read; the same holds for dP^T / dS^T.
+// Order of the GEMMs: the next pair's S^T overwrites P^T, so it waits for this
+// pair's dV; the next dP^T waits for this pair's dK.  Two threads issue: one
+// S^T then dV, the other dP^T then dK, so the tensor pipe sees dV(i), dK(i),
+// S^T(i+1), dP^T(i+1), ...: each GEMM's wait is covered by the one before it
+// (the threads compute P^T(i+1) while dP^T(i+1) runs, and dS^T(i+1) while
+// dV(i+1) runs).
 // Warp roles: warps 0-7 compute (warp w: TMEM lane quarter w % 4 = key rows,
-// query columns 32 (w / 4) ..; two warps per SM sub-partition hide each
+// query columns 64 (w / 4) ..; two warps per SM sub-partition hide each
 // other's latencies), warp 8 loads with TMA (Q, dO and the tile's 16-byte row
-// records {lse*log2e, Delta, key limit}) into a 4-stage ring, and three warps
-// each have one thread issue one kind of GEMM: warp 9 (which owns TMEM) S^T,
-// warp 11 dP^T, warp 10 dV and dK.  One tcgen05.mma costs the issuing thread
-// about as long as the tensor cores take to run an N=64 one, so a single
-// issuer, which also waits on the compute warps between groups, cannot keep
-// the queue full; three can.  Each thread's commits track its own GEMMs.
-// All waits are bounded.
+// records {-lse*log2e, Delta, key limit}) into a ring of stages, warp 9 (which
+// owns TMEM) issues S^T and dV, warp 10 dP^T and dK.  Each thread's commits
+// track its own GEMMs.  All waits are bounded.
 // Clusters: BA_BWD_CS CTAs that own consecutive key tiles of one chunk (and
 // one kv head) form a thread-block cluster, which only makes the hardware run
 // them side by side.  They meet the same query tiles in the same order and
@@ -66,18 +65,19 @@
 namespace {
 
 constexpr int KBN = 128;  // keys per CTA
-constexpr int QBM = 64;   // queries per tile
-constexpr int NTHREADS = 384;  // 8 compute warps, 1 TMA warp, 3 MMA-issuing warps
+constexpr int QBM = BA_BWD_BM;  // queries per tile (128)
+constexpr int NTHREADS = 352;  // 8 compute warps, 1 TMA warp, 2 MMA-issuing warps
+static_assert(QBM == 128, "the GEMM shapes below assume 128-query tiles");
 
-constexpr int NQS = 4;    // query-tile pipeline stages
 constexpr int CS = BA_BWD_CS;
 
 template <int D>
 struct BwdSmem {
   static constexpr int CB = D / 64;            // 64-column (128-byte) blocks per row
+  static constexpr int NQS = D == 128 ? 2 : 4; // query-tile pipeline stages
   static constexpr uint32_t KT = 128u * 128u;  // [128 keys][64 d] bf16 block
-  static constexpr uint32_t QT = 64u * 128u;   // [64 queries][64 d] bf16 block
-  static constexpr uint32_t META = 64 * 16;    // 64 row records {lse*log2e, Delta, limit, 0}
+  static constexpr uint32_t QT = 128u * 128u;  // [128 queries][64 d] bf16 block
+  static constexpr uint32_t META = QBM * 16;   // row records {-lse*log2e, Delta, limit, 0}
   static constexpr uint32_t k = 0;             // CB blocks
   static constexpr uint32_t v = k + CB * KT;
   static constexpr uint32_t q = v + CB * KT;   // [NQS stages][CB blocks]
@@ -87,23 +87,22 @@ struct BwdSmem {
   static constexpr uint32_t bytes = bars + 256;
   static constexpr uint32_t alloc = bytes + 1024;
 };
+static_assert(BwdSmem<128>::alloc <= 227u * 1024u && BwdSmem<64>::alloc <= 227u * 1024u, "shared memory");
 
 enum {
   B_KV = 0,                    // K and V are in shared memory
-  B_KT = 1,                    // K is in TMEM (one arrival per compute warp)
-  B_QFULL = 2,                 // [NQS]
-  B_QFREE = B_QFULL + NQS,     // [NQS] the dV / dK GEMMs have read the stage
-  B_SFULL = B_QFREE + NQS,     // S^T of a pair is in TMEM
-  B_SEMPTY = B_SFULL + 1,      // the threads have loaded the S^T buffer
-  B_DPFULL = B_SEMPTY + 1,     // dP^T of a pair is in TMEM
-  B_DPEMPTY = B_DPFULL + 1,    // the threads have loaded the dP^T buffer
-  B_PFULL = B_DPEMPTY + 1,     // P^T is in the P/dS buffer
-  B_DSFULL = B_PFULL + 1,      // dS^T is in the P/dS buffer
-  B_PDSEMPTY = B_DSFULL + 1,   // dV/dK of the pair have read the P/dS buffer
-  B_DONE = B_PDSEMPTY + 1,
-  B_COUNT = B_DONE + 1
+  B_SFULL = 1,                 // S^T of a pair is in TMEM
+  B_SFREE = 2,                 // dV of a pair has read P^T: the S^T buffer is free
+  B_DPFULL = 3,                // dP^T of a pair is in TMEM
+  B_DPFREE = 4,                // dK of a pair has read dS^T: the dP^T buffer is free
+  B_PFULL = 5,                 // P^T is in TMEM (one arrival per compute warp)
+  B_DSFULL = 6,                // dS^T is in TMEM (one arrival per compute warp)
+  B_DONE = 7,                  // both issuers' last GEMMs have completed
+  B_QFULL = 8,                 // [NQS]
+  // B_QFREE = B_QFULL + NQS   // [NQS] the pair's dV and dK have read the stage
 };
-static_assert(8 * B_COUNT + 16 <= 256, "barrier area");
+__host__ __device__ constexpr int b_count(int nqs) { return B_QFULL + 2 * nqs; }
+static_assert(8 * b_count(4) + 16 <= 256, "barrier area");
 
 // Iteration of one key tile over (phase, stream, query range, query tile).
 // Phase 0 covers the unmasked ranges (every range but the last when the last
@@ -156,6 +155,43 @@ struct QIter {
   }
 };
 
+// Packed arithmetic of the compute warps.  P^T and dS^T are GEMM operands in
+// bf16, so they are formed two at a time in bf16x2: one fp32x2 FMA for the
+// exponent, rounded to bf16x2, one ex2.bf16x2 (two exponentials per MUFU
+// instruction), and dS^T = P^T (dP^T - Delta) as one fp32x2 subtraction,
+// rounded, times P^T in bf16x2.  The first element of each pair is in the low
+// half, which is the column order of a packed TMEM operand.
+__device__ __forceinline__ uint32_t fma2_bf16x2(float a0, float a1, float b, float c0, float c1) {
+  uint32_t h;
+  asm("{\n .reg .b64 a, bb, cc, d;\n .reg .f32 d0, d1;\n"
+      " mov.b64 a, {%1, %2};\n mov.b64 bb, {%3, %3};\n mov.b64 cc, {%4, %5};\n"
+      " fma.rn.f32x2 d, a, bb, cc;\n mov.b64 {d0, d1}, d;\n"
+      " cvt.rn.bf16x2.f32 %0, d1, d0;\n}\n"
+      : "=r"(h)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+  return h;
+}
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t sub2_bf16x2(float a0, float a1, float b0, float b1) {
+  uint32_t h;
+  asm("{\n .reg .b64 a, b, d;\n .reg .f32 d0, d1;\n"
+      " mov.b64 a, {%1, %2};\n mov.b64 b, {%3, %4};\n"
+      " sub.rn.f32x2 d, a, b;\n mov.b64 {d0, d1}, d;\n"
+      " cvt.rn.bf16x2.f32 %0, d1, d0;\n}\n"
+      : "=r"(h)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+  return h;
+}
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
     main_bwd_kv_tc_kernel(const BaBwdArgs a, const __grid_constant__ CUtensorMap tmq,
@@ -163,6 +199,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                           const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmrec) {
   using L = BwdSmem<D>;
   constexpr int CB = L::CB;
+  constexpr int NQS = L::NQS;
+  constexpr int B_QFREE = B_QFULL + NQS;
+  constexpr int B_COUNT = b_count(NQS);
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -190,19 +229,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(bar(B_KV), 1);
-    mbar_init(bar(B_KT), 8);
-    for (int s = 0; s < NQS; ++s) {
-      mbar_init(bar(B_QFULL + s), 1);
-      mbar_init(bar(B_QFREE + s), 1);
-    }
     mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_SEMPTY), 8);  // one arrival per compute warp
+    mbar_init(bar(B_SFREE), 1);
     mbar_init(bar(B_DPFULL), 1);
-    mbar_init(bar(B_DPEMPTY), 8);
+    mbar_init(bar(B_DPFREE), 1);
     mbar_init(bar(B_PFULL), 8);
     mbar_init(bar(B_DSFULL), 8);
-    mbar_init(bar(B_PDSEMPTY), 1);
-    mbar_init(bar(B_DONE), 1);
+    mbar_init(bar(B_DONE), 2);
+    for (int s = 0; s < NQS; ++s) {
+      mbar_init(bar(B_QFULL + s), 1);
+      mbar_init(bar(B_QFREE + s), 2);  // one commit from each issuer
+    }
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -213,8 +250,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tK = tmem, tS = tmem + 64, tDP = tmem + 128, tPD = tmem + 192, tDK = tmem + 256, tDV = tmem + 256 + D;
+  const uint32_t tS = tmem, tDP = tmem + 128, tDK = tmem + 256, tDV = tmem + 256 + D;
   const bool any = kt.nqr > 0;
+  // pairs this CTA visits
+  int npairs = 0;
+  for (int r = kt.qr0; r < kt.qr0 + kt.nqr; ++r) npairs += (tb.bqr[r].t1 - tb.bqr[r].t0) * nstream;
 
   if (warp == 8) {
     // ------------------------------------------------------------ loads
@@ -231,8 +271,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tma_load_3d(sbase + L::v + cb * L::KT, &tmv, bar(B_KV), cb * 64, kvh, kt.pos0);
         }
       }
-    }
-    if (lane == 0) {
       // Q / dO rows and the record row of pair state `q`
       auto coords = [&](const QIter& q, int& h, int& qrow, int& srow) {
         const BaQTile qt = tb.bq[q.ti];
@@ -243,15 +281,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       };
       QIter it;
       it.init(tb.bqr, kt.qr0, kt.nqr, nstream);
-      int i = 0;
-      bool pok = true;
       int h = 0, qrow = 0, srow = 0;
       if (it.valid()) coords(it, h, qrow, srow);
-      for (; it.valid(); ++i) {
+      for (int i = 0; it.valid(); ++i) {
         const int st = i % NQS;
-        const uint32_t ph = (i / NQS) & 1;
         // pair i - NQS has left the stage
-        if (!mbar_wait(bar(B_QFREE + st), ph ^ 1, tb.status, abort_flag)) { pok = false; break; }
+        if (!mbar_wait(bar(B_QFREE + st), ((i / NQS) & 1) ^ 1, tb.status, abort_flag)) break;
         const uint32_t fb = bar(B_QFULL + st);
         mbar_expect_tx(fb, 2 * CB * L::QT + L::META);
         // the stage's boxes: Q and dO in CB 64-column blocks each, the row records
@@ -264,70 +299,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         it.next();
         if (it.valid()) coords(it, h, qrow, srow);
       }
-      (void)pok;
     }
-  } else if (warp == 9 || warp == 11) {
-    // ------------------------------------------------------------ S^T (warp 9) / dP^T (warp 11) issuers
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ issuers
+    // warp 9: S^T = K Q^T, then dV += P^T dO;  warp 10: dP^T = V dO^T, then dK += dS^T Q
     if (elect_one() && any) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, QBM, false, false);
-      int n = 0;
-      for (int r = kt.qr0; r < kt.qr0 + kt.nqr; ++r) n += (tb.bqr[r].t1 - tb.bqr[r].t0) * nstream;
+      constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
       const bool is_s = warp == 9;
       // operand descriptors, built once: every MMA below adds a constant offset
-      const uint64_t da = smem_desc_sw128(sbase + L::v, 16, 1024);  // V (the dP^T GEMM's A)
-      const uint64_t db = smem_desc_sw128(sbase + (is_s ? L::q : L::go), 16, 1024);
-      const uint32_t td = is_s ? tS : tDP;
-      const int full_bar = is_s ? B_SFULL : B_DPFULL, free_bar = is_s ? B_SEMPTY : B_DPEMPTY;
-      // S^T reads K from TMEM once the threads have copied it there
-      bool ok = mbar_wait(bar(is_s ? B_KT : B_KV), 0, tb.status, abort_flag);
-      for (int i = 0; ok && i < n; ++i) {
+      const uint64_t da = smem_desc_sw128(sbase + (is_s ? L::k : L::v), 16, 1024);  // K or V (K-major A)
+      const uint64_t db = smem_desc_sw128(sbase + (is_s ? L::q : L::go), 16, 1024);  // Q or dO (K-major B)
+      // dV reads dO, dK reads Q, both as MN-major B operands (N = d)
+      const uint64_t dm = smem_desc_sw128(sbase + (is_s ? L::go : L::q), L::QT, 1024);
+      const uint32_t t_first = is_s ? tS : tDP;    // S^T / dP^T, then P^T / dS^T over it
+      const uint32_t t_acc = is_s ? tDV : tDK;
+      const int full_bar = is_s ? B_SFULL : B_DPFULL, free_bar = is_s ? B_SFREE : B_DPFREE;
+      const int ready_bar = is_s ? B_PFULL : B_DSFULL;
+      bool ok = mbar_wait(bar(B_KV), 0, tb.status, abort_flag);
+      for (int i = 0; ok && i < npairs; ++i) {
         const int qs = i % NQS;
         if (!mbar_wait(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) break;
-        // one buffer: pair i - 1's values have been loaded by the threads
-        if (!mbar_wait(bar(free_bar), (i & 1) ^ 1, tb.status, abort_flag)) break;
+        // the buffer is free once pair i - 1's dV (dK) has read what the threads wrote over it
+        if (i > 0 && !mbar_wait(bar(free_bar), (i - 1) & 1, tb.status, abort_flag)) break;
         tc_fence_after();
         const uint64_t dbs = desc_add(db, qs * CB * L::QT);
-        if (is_s) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)  // a k16 step of K spans 8 TMEM columns
-            tc_mma_tmem_a(td, tK + kk * 8, desc_add(dbs, (kk >> 2) * L::QT + (kk & 3) * 32), id_s, kk > 0);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma(td, desc_add(da, (kk >> 2) * L::KT + (kk & 3) * 32), desc_add(dbs, (kk >> 2) * L::QT + (kk & 3) * 32),
-                   id_s, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma(t_first, desc_add(da, (kk >> 2) * L::KT + (kk & 3) * 32),
+                 desc_add(dbs, (kk >> 2) * L::QT + (kk & 3) * 32), id_s, kk > 0);
         tc_commit(bar(full_bar));
-      }
-    }
-  } else if (warp == 10) {
-    // ------------------------------------------------------------ dV / dK issuer
-    if (elect_one() && any) {
-      constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
-      int n = 0;
-      for (int r = kt.qr0; r < kt.qr0 + kt.nqr; ++r) n += (tb.bqr[r].t1 - tb.bqr[r].t0) * nstream;
-      const uint64_t dqm = smem_desc_sw128(sbase + L::q, L::QT, 1024), dgm = smem_desc_sw128(sbase + L::go, L::QT, 1024);
-      for (int i = 0; i < n; ++i) {
-        const int qs = i % NQS;
-        const uint32_t pa = tPD, ph = i & 1;
-        // dV += P^T dO as soon as P^T is in TMEM
-        if (!mbar_wait(bar(B_PFULL), ph, tb.status, abort_flag)) break;
+        // P^T (dS^T) written by the threads
+        if (!mbar_wait(bar(ready_bar), i & 1, tb.status, abort_flag)) break;
         tc_fence_after();
-        const uint64_t dgs = desc_add(dgm, qs * CB * L::QT);
-#pragma unroll
-        for (int kk = 0; kk < QBM / 16; ++kk)  // queries 16 kk .. 16 kk + 15 sit in query half kk / 2
-          tc_mma_tmem_a(tDV, pa + (kk >> 1) * 32 + (kk & 1) * 8, desc_add(dgs, kk * 2048), id_kv,
-                        (i > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q once the threads have written dS^T
-        if (!mbar_wait(bar(B_DSFULL), ph, tb.status, abort_flag)) break;
-        tc_fence_after();
-        const uint64_t dqs = desc_add(dqm, qs * CB * L::QT);
+        const uint64_t dms = desc_add(dm, qs * CB * L::QT);
+        // queries 16 kk .. 16 kk + 15 sit in query half kk / 4, columns 8 (kk % 4) ..
 #pragma unroll
         for (int kk = 0; kk < QBM / 16; ++kk)
-          tc_mma_tmem_a(tDK, pa + (kk >> 1) * 32 + (kk & 1) * 8 + 16, desc_add(dqs, kk * 2048), id_kv,
+          tc_mma_tmem_a(t_acc, t_first + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(dms, kk * 2048), id_kv,
                         (i > 0 || kk > 0) ? 1u : 0u);
-        // the pair's last readers of its P/dS buffer and its Q / dO stage
-        tc_commit(bar(B_PDSEMPTY));
+        tc_commit(bar(free_bar));
         tc_commit(bar(B_QFREE + qs));
       }
       tc_commit(bar(B_DONE));
@@ -335,107 +346,78 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp < 8) {
     // ------------------------------------------------------------ compute
     // warp w: TMEM lane quarter w % 4 (key rows 32 (w % 4) ..), query columns
-    // 32 (w / 4) .. 32 (w / 4) + 31 of each 64-query tile
+    // 64 (w / 4) .. 64 (w / 4) + 63 of each 128-query tile
     const int quarter = warp & 3, half = warp >> 2;
     const int row = quarter * 32 + lane;
-    const int col0 = half * 32;
+    const int col0 = half * 64;
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const bool kok = row < kt.nkeys;
     const int kpos = kt.pos0 + row;
-    // K into TMEM as the S^T GEMM's A operand: this thread's key row, d block
-    // `half` (128 bytes, 16-byte chunks at chunk ^ (row % 8) in the 128-byte
-    // swizzled tile) -> columns 32 half .. 32 half + 31, two d values each;
-    // with d = 64 the warps of the second half have nothing to copy
-    if (any) {
-      if (!mbar_wait_warp(bar(B_KV), 0, tb.status, abort_flag)) {
-        // fall through: the issuers see the abort flag and skip their GEMMs
-      } else if (half >= CB) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_KT));
-      } else {
-        const unsigned char* krow = gbase + L::k + half * L::KT + row * 128;
-        uint32_t w[32];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 v = *reinterpret_cast<const uint4*>(krow + ((j ^ (row & 7)) * 16));
-          w[4 * j] = v.x;
-          w[4 * j + 1] = v.y;
-          w[4 * j + 2] = v.z;
-          w[4 * j + 3] = v.w;
-        }
-        tmem_st32u(tK + lane_off + half * 32, w);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_KT));
-      }
-    }
     QIter it;
     it.init(tb.bqr, kt.qr0, kt.nqr, nstream);
     bool ok = true;
     int i = 0;
     for (; it.valid(); ++i, it.next()) {
       const int qs = i % NQS;
-      const uint32_t pd = tPD + lane_off + col0;  // this warp's columns of the P/dS buffer
+      const uint32_t ph = i & 1;
       const int nrows = tb.bq[it.ti].nrows;
       const bool diag = it.cur.diag != 0;
       // q_full: the row records of this tile are in shared memory
       if (!mbar_wait_warp(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) { ok = false; break; }
-      if (!mbar_wait_warp(bar(B_SFULL), i & 1, tb.status, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(B_SFULL), ph, tb.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      float p[32];
+      float p[64];
       tmem_ld32(tS + lane_off + col0, p);
+      tmem_ld32(tS + lane_off + col0 + 32, p + 32);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SEMPTY));  // the next pair's S^T GEMM may start
-      // row records {lse*log2e, Delta, limit, 0}; queries past the tile are masked
+      // row records {-lse*log2e, Delta, limit, 0}; queries past the tile are masked
       const uint32_t rec = sbase + L::meta + qs * L::META + 16 * col0;
       const int nq = nrows - col0;
-      float delta[32];
-      if (!diag && kok && nq >= 32) {
-        // full tile (the common case): no mask, one 8-byte load per column
+      uint32_t pb[32];  // P^T, bf16 pairs
+      if (!diag && kok && nq >= 64) {
+        // full tile (the common case): no mask
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 r = lds_f2(rec + 16 * c);
-          p[c] = ex2_approx(fmaf(p[c], sh.scale_log2, -r.x));
-          delta[c] = r.y;
+        for (int c = 0; c < 64; c += 2) {
+          const float2 r0 = lds_f2(rec + 16 * c), r1 = lds_f2(rec + 16 * (c + 1));
+          pb[c >> 1] = ex2_bf16x2(fma2_bf16x2(p[c], p[c + 1], sh.scale_log2, r0.x, r1.x));
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float4 r = lds_f4(rec + 16 * c);
-          const bool v = kok && c < nq && (!diag || kpos <= __float_as_int(r.z));
-          const float e = ex2_approx(fmaf(p[c], sh.scale_log2, -r.x));
-          p[c] = v ? e : 0.f;
-          delta[c] = r.y;
+        for (int c = 0; c < 64; c += 2) {
+          const float4 r0 = lds_f4(rec + 16 * c), r1 = lds_f4(rec + 16 * (c + 1));
+          const bool v0 = kok && c < nq && (!diag || kpos <= __float_as_int(r0.z));
+          const bool v1 = kok && c + 1 < nq && (!diag || kpos <= __float_as_int(r1.z));
+          const float e0 = ex2_approx(fmaf(p[c], sh.scale_log2, r0.x));
+          const float e1 = ex2_approx(fmaf(p[c + 1], sh.scale_log2, r1.x));
+          pb[c >> 1] = pack_bf16(v0 ? e0 : 0.f, v1 ? e1 : 0.f);
         }
       }
-      uint32_t w[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) w[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
-      // P^T into the P/dS buffer once pair i - 1's dV / dK GEMMs have read it
-      if (!mbar_wait_warp(bar(B_PDSEMPTY), (i & 1) ^ 1, tb.status, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      tmem_st16(pd, w);
+      // P^T over the first 32 of this warp's 64 columns of the S^T buffer
+      tmem_st16(tS + lane_off + col0, pb);
+      tmem_st16(tS + lane_off + col0 + 16, pb + 16);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL));
-      // dS^T = P^T (dP^T - Delta)
-      if (!mbar_wait_warp(bar(B_DPFULL), i & 1, tb.status, abort_flag)) { ok = false; break; }
+      // dS^T = P^T (dP^T - Delta), over the first 32 of this warp's columns of
+      // the dP^T buffer: columns 0..31 are loaded before 0..15 are written,
+      // 32..63 before 16..31
+      if (!mbar_wait_warp(bar(B_DPFULL), ph, tb.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      float dp[32];
-      tmem_ld32(tDP + lane_off + col0, dp);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DPEMPTY));  // the next pair's dP^T GEMM may start
 #pragma unroll
-      for (int c = 0; c < 32; ++c) dp[c] = p[c] * (dp[c] - delta[c]);
+      for (int g = 0; g < 2; ++g) {
+        float dp[32];
+        tmem_ld32(tDP + lane_off + col0 + 32 * g, dp);
+        tmem_wait_ld();
+        uint32_t w[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) w[e] = pack_bf16(dp[2 * e], dp[2 * e + 1]);
-      tmem_st16(pd + 16, w);
+        for (int e = 0; e < 16; ++e) {
+          const int c = 32 * g + 2 * e;
+          const float d0 = lds_f2(rec + 16 * c).y, d1 = lds_f2(rec + 16 * (c + 1)).y;
+          w[e] = mul_bf16x2(pb[16 * g + e], sub2_bf16x2(dp[2 * e], dp[2 * e + 1], d0, d1));
+        }
+        tmem_st16(tDP + lane_off + col0 + 16 * g, w);
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

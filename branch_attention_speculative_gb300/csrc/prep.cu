@@ -1,7 +1,7 @@
 // K5 — backward preprocessing.
 //
 // For every query-head row: Delta = <dO, O> in fp32 (the row term of the
-// softmax backward, dS = P * (dP - Delta)).  lse (in base 2), Delta and the
+// softmax backward, dS = P * (dP - Delta)).  -lse (in base 2), Delta and the
 // row's main-key limit go into one 16-byte record per (step, head, row), in
 // natural row order and stream-major, so that the records of a query tile (a
 // run of consecutive natural rows) are one contiguous TMA box.  The pages only
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BaBwdArgs a) {
     if (!valid) continue;
     if (sub == 0) {  // one 16-byte record per (step, head, row), stream-major
       const int64_t srow = (j * sh.Hq + h) * sh.rows + r;
-      a.rowrec[srow] = make_float4(a.lse[row] * BA_LOG2E, acc, __int_as_float(a.tb.nat_lim[r]), 0.f);
+      a.rowrec[srow] = make_float4(-a.lse[row] * BA_LOG2E, acc, __int_as_float(a.tb.nat_lim[r]), 0.f);
     }
   }
 }

@@ -132,7 +132,7 @@ SMALL = [
     W.small("causal", [136, 8, 256], heads_q=4, heads_kv=4, head_dim=64, cp=2, seed=5, name="causal_mha"),
     W.small("block", [64], heads_q=2, heads_kv=1, head_dim=64, cp=2, block=1, anchors_per_seq=1, seed=6,
             name="block_one_anchor"),
-    # chunks of several whole 128-key / 64- and 128-query tiles plus a ragged
+    # chunks of several whole 128-key / 128-query tiles plus a ragged
     # tail, at head_dim 128: every main key's dK/dV, including the unmasked
     # key tiles away from the diagonal, is checked against the full oracle
     W.small("ttt", [1280, 768], heads_q=8, heads_kv=2, head_dim=128, cp=2, depth=2, seed=7,
@@ -144,6 +144,8 @@ SMALL = [
             name="block64_c2"),
     W.small("ttt", [128, 64], heads_q=2, heads_kv=1, head_dim=128, cp=2, depth=16, seed=11, name="ttt_depth16"),
     W.small("causal", [384, 640], heads_q=4, heads_kv=2, head_dim=128, cp=2, seed=9, name="causal_d128_gqa"),
+    # head_dim 128, one q head per kv head and an odd number of query streams
+    W.small("ttt", [256, 96], heads_q=3, heads_kv=3, head_dim=128, cp=2, depth=3, seed=12, name="ttt_d128_odd_streams"),
 ]
 
 

@@ -221,7 +221,7 @@ def _backward_cover(wl, lim, bq, bkv, br):
         for t0, t1, diag, _ in br[qr0:qr0 + nqr]:
             for t in range(t0, t1):
                 rows, rl = _tile_rows(bq[t], lim)
-                assert 0 < len(rows) <= 64
+                assert 0 < len(rows) <= 128
                 vis = keys[None, :] <= rl[:, None]
                 if not diag:
                     assert vis.all()
