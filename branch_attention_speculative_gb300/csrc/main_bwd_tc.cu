@@ -83,7 +83,11 @@ struct BwdSmem {
   static constexpr uint32_t q = v + CB * KT;   // [NQS stages][CB blocks]
   static constexpr uint32_t go = q + NQS * CB * QT;
   static constexpr uint32_t meta = go + NQS * CB * QT;  // [NQS stages]
-  static constexpr uint32_t bars = meta + NQS * META;
+  // the stage's -lse*log2e and Delta as two planes of 128 floats, so that a
+  // thread reads four columns' values with one 16-byte load
+  static constexpr uint32_t PLANES = 2 * QBM * 4;
+  static constexpr uint32_t planes = meta + NQS * META;  // [NQS stages]
+  static constexpr uint32_t bars = planes + NQS * PLANES;
   static constexpr uint32_t bytes = bars + 256;
   static constexpr uint32_t alloc = bytes + 1024;
 };
@@ -100,8 +104,9 @@ enum {
   B_DONE = 7,                  // both issuers' last GEMMs have completed
   B_QFULL = 8,                 // [NQS]
   // B_QFREE = B_QFULL + NQS   // [NQS] the pair's dV and dK have read the stage
+  // B_RFULL = B_QFULL + 2 NQS // [NQS] the stage's record planes are written
 };
-__host__ __device__ constexpr int b_count(int nqs) { return B_QFULL + 2 * nqs; }
+__host__ __device__ constexpr int b_count(int nqs) { return B_QFULL + 3 * nqs; }
 static_assert(8 * b_count(4) + 16 <= 256, "barrier area");
 
 // Iteration of one key tile over (phase, stream, query range, query tile).
@@ -201,6 +206,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   constexpr int CB = L::CB;
   constexpr int NQS = L::NQS;
   constexpr int B_QFREE = B_QFULL + NQS;
+  constexpr int B_RFULL = B_QFULL + 2 * NQS;
   constexpr int B_COUNT = b_count(NQS);
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -239,6 +245,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int s = 0; s < NQS; ++s) {
       mbar_init(bar(B_QFULL + s), 1);
       mbar_init(bar(B_QFREE + s), 2);  // one commit from each issuer
+      mbar_init(bar(B_RFULL + s), 1);
     }
     fence_mbar_init();
   }
@@ -271,34 +278,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tma_load_3d(sbase + L::v + cb * L::KT, &tmv, bar(B_KV), cb * 64, kvh, kt.pos0);
         }
       }
-      // Q / dO rows and the record row of pair state `q`
-      auto coords = [&](const QIter& q, int& h, int& qrow, int& srow) {
-        const BaQTile qt = tb.bq[q.ti];
-        const int j = q.sx / sh.G;
-        h = kvh * sh.G + q.sx % sh.G;
-        qrow = int(int64_t(j) * sh.rows + qt.nrow0);
-        srow = int((int64_t(j) * sh.Hq + h) * sh.rows + qt.nrow0);
-      };
-      QIter it;
-      it.init(tb.bqr, kt.qr0, kt.nqr, nstream);
-      int h = 0, qrow = 0, srow = 0;
-      if (it.valid()) coords(it, h, qrow, srow);
-      for (int i = 0; it.valid(); ++i) {
-        const int st = i % NQS;
+    }
+    // Q / dO rows and the record row of pair state `q`
+    auto coords = [&](const QIter& q, int& h, int& qrow, int& srow) {
+      const BaQTile qt = tb.bq[q.ti];
+      const int j = q.sx / sh.G;
+      h = kvh * sh.G + q.sx % sh.G;
+      qrow = int(int64_t(j) * sh.rows + qt.nrow0);
+      srow = int((int64_t(j) * sh.Hq + h) * sh.rows + qt.nrow0);
+    };
+    QIter it;
+    it.init(tb.bqr, kt.qr0, kt.nqr, nstream);
+    int h = 0, qrow = 0, srow = 0;
+    if (it.valid()) coords(it, h, qrow, srow);
+    for (int i = 0; it.valid(); ++i) {
+      const int st = i % NQS;
+      const uint32_t fb = bar(B_QFULL + st);
+      bool ok = true;
+      if (lane == 0) {
         // pair i - NQS has left the stage
-        if (!mbar_wait(bar(B_QFREE + st), ((i / NQS) & 1) ^ 1, tb.status, abort_flag)) break;
-        const uint32_t fb = bar(B_QFULL + st);
-        mbar_expect_tx(fb, 2 * CB * L::QT + L::META);
-        // the stage's boxes: Q and dO in CB 64-column blocks each, the row records
-        for (int cb = 0; cb < CB; ++cb) {
-          tma_load_3d(sbase + L::q + (st * CB + cb) * L::QT, &tmq, fb, cb * 64, h, qrow);
-          tma_load_3d(sbase + L::go + (st * CB + cb) * L::QT, &tmdo, fb, cb * 64, h, qrow);
+        ok = mbar_wait(bar(B_QFREE + st), ((i / NQS) & 1) ^ 1, tb.status, abort_flag);
+        if (ok) {
+          mbar_expect_tx(fb, 2 * CB * L::QT + L::META);
+          // the stage's boxes: Q and dO in CB 64-column blocks each, the row records
+          for (int cb = 0; cb < CB; ++cb) {
+            tma_load_3d(sbase + L::q + (st * CB + cb) * L::QT, &tmq, fb, cb * 64, h, qrow);
+            tma_load_3d(sbase + L::go + (st * CB + cb) * L::QT, &tmdo, fb, cb * 64, h, qrow);
+          }
+          tma_load_2d(sbase + L::meta + st * L::META, &tmrec, fb, 0, srow);
         }
-        tma_load_2d(sbase + L::meta + st * L::META, &tmrec, fb, 0, srow);
-        // the next pair's table entry is read while this stage's loads fly
-        it.next();
-        if (it.valid()) coords(it, h, qrow, srow);
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      // the next pair's table entry is read while this stage's loads fly
+      it.next();
+      if (it.valid()) coords(it, h, qrow, srow);
+      // the records as planes: lane l moves columns 4l .. 4l + 3
+      if (!mbar_wait_warp(fb, (i / NQS) & 1, tb.status, abort_flag)) break;
+      const uint32_t rec = sbase + L::meta + st * L::META + 64 * lane;
+      const float4 r0 = lds_f4(rec), r1 = lds_f4(rec + 16), r2 = lds_f4(rec + 32), r3 = lds_f4(rec + 48);
+      float4* pl = reinterpret_cast<float4*>(gbase + L::planes + st * L::PLANES);
+      pl[lane] = make_float4(r0.x, r1.x, r2.x, r3.x);
+      pl[QBM / 4 + lane] = make_float4(r0.y, r1.y, r2.y, r3.y);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_RFULL + st));
     }
   } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------ issuers
@@ -362,8 +384,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t ph = i & 1;
       const int nrows = tb.bq[it.ti].nrows;
       const bool diag = it.cur.diag != 0;
-      // q_full: the row records of this tile are in shared memory
-      if (!mbar_wait_warp(bar(B_QFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) { ok = false; break; }
+      // the row records of this tile (and their planes) are in shared memory
+      if (!mbar_wait_warp(bar(B_RFULL + qs), (i / NQS) & 1, tb.status, abort_flag)) { ok = false; break; }
       if (!mbar_wait_warp(bar(B_SFULL), ph, tb.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
       float p[64];
@@ -372,14 +394,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_wait_ld();
       // row records {-lse*log2e, Delta, limit, 0}; queries past the tile are masked
       const uint32_t rec = sbase + L::meta + qs * L::META + 16 * col0;
+      const uint32_t pln = sbase + L::planes + qs * L::PLANES + 4 * col0;  // -lse*log2e; Delta at + 4 QBM
       const int nq = nrows - col0;
       uint32_t pb[32];  // P^T, bf16 pairs
       if (!diag && kok && nq >= 64) {
         // full tile (the common case): no mask
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float2 r0 = lds_f2(rec + 16 * c), r1 = lds_f2(rec + 16 * (c + 1));
-          pb[c >> 1] = ex2_bf16x2(fma2_bf16x2(p[c], p[c + 1], sh.scale_log2, r0.x, r1.x));
+        for (int c = 0; c < 64; c += 4) {
+          const float4 n = lds_f4(pln + 4 * c);
+          pb[c >> 1] = ex2_bf16x2(fma2_bf16x2(p[c], p[c + 1], sh.scale_log2, n.x, n.y));
+          pb[(c >> 1) + 1] = ex2_bf16x2(fma2_bf16x2(p[c + 2], p[c + 3], sh.scale_log2, n.z, n.w));
         }
       } else {
 #pragma unroll
@@ -411,10 +435,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_wait_ld();
         uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = 32 * g + 2 * e;
-          const float d0 = lds_f2(rec + 16 * c).y, d1 = lds_f2(rec + 16 * (c + 1)).y;
-          w[e] = mul_bf16x2(pb[16 * g + e], sub2_bf16x2(dp[2 * e], dp[2 * e + 1], d0, d1));
+        for (int e = 0; e < 16; e += 2) {
+          const float4 d4 = lds_f4(pln + 4 * QBM + 4 * (32 * g + 2 * e));
+          w[e] = mul_bf16x2(pb[16 * g + e], sub2_bf16x2(dp[2 * e], dp[2 * e + 1], d4.x, d4.y));
+          w[e + 1] = mul_bf16x2(pb[16 * g + e + 1], sub2_bf16x2(dp[2 * e + 2], dp[2 * e + 3], d4.z, d4.w));
         }
         tmem_st16(tDP + lane_off + col0 + 16 * g, w);
       }
