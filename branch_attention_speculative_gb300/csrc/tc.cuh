@@ -99,11 +99,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
 }
 
 // Loads from a 32-bit shared-memory address (ld.shared, never the generic path).
-__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];\n" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
@@ -152,11 +147,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
       "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
-}
-
-// 32 consecutive 32-bit columns of this thread's TMEM lane, raw words.
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* r) {
-  tmem_st32(taddr, reinterpret_cast<const float*>(r));
 }
 
 // 16 consecutive 32-bit columns of this thread's TMEM lane (e.g. 32 bf16 packed in pairs).
