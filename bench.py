@@ -331,6 +331,15 @@ def run_ours(args, rank, world, local):
                         "traffic": measured_traffic(dom, wl.name),
                         "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                         "peak_source": f"bf16_tflops_sustained ({peaks['source']})"}
+            if clocks.get("sm_mhz"):
+                # The measured peak ran at its own clock; this is the dense bf16
+                # rate of the tensor pipes at this run's median SM clock: 8192
+                # FLOP per clock per SM (one M=128, N=128, K=16 MMA every 64
+                # cycles, measured) times the SMs.
+                sms = torch.cuda.get_device_properties(local).multi_processor_count
+                at_clock = 8192.0 * sms * clocks["sm_mhz"] * 1e6 / 1e12
+                roofline["peak_at_clock"] = at_clock
+                roofline["frac_at_clock"] = e["achieved"] / at_clock
         else:
             roofline = {"kernel": dom, "bound": "hbm", "achieved": e["achieved"], "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": e["achieved"] / peaks["hbm_gbs"], "traffic": None,
