@@ -157,6 +157,26 @@ def test_null_and_misaligned_pointers_rejected_before_launch(api):
     assert lib.ba_lse_merge(4, 96, None, None, None, None, None, None, None) == -1
 
 
+def test_step_and_8bit_arguments_rejected_before_launch(api):
+    """The per-step TTT calls and the 8-bit forward check their arguments before
+    anything is enqueued (fake, aligned, never dereferenced pointers)."""
+    lib = api.lib()
+    ptr = ctypes.c_void_p(0x1000)
+    ttt = api.Plan("ttt", [0, 64], 2, 1, 64, 2, ttt_depth=2)
+    for step in (-1, 2, 7):  # slots are 0 .. depth - 1
+        assert lib.ba_forward_step(ttt._h, step, *([ptr] * 7), ptr, 1 << 30, None) == -1
+        assert lib.ba_backward_step(ttt._h, step, *([ptr] * 14), 1 << 30, None) == -1
+    block = api.Plan("block", [0, 64], 2, 1, 64, 2, block_size=4, anchors=[3, 40])
+    assert lib.ba_forward_step(block._h, 0, *([ptr] * 7), ptr, 1 << 30, None) == -1
+    assert lib.ba_backward_step(block._h, 0, *([ptr] * 14), 1 << 30, None) == -1
+    # a valid step with a null input, a misaligned output, no workspace
+    assert lib.ba_forward_step(ttt._h, 1, None, *([ptr] * 6), ptr, 1 << 30, None) == -1
+    assert lib.ba_forward_step(ttt._h, 1, *([ptr] * 5), ctypes.c_void_p(0x1004), ptr, ptr, 1 << 30, None) == -1
+    assert lib.ba_forward_step(ttt._h, 1, *([ptr] * 7), None, 0, None) == -6
+    # the 8-bit forward is built for head_dim 128 only
+    assert lib.ba_forward_fp8(ttt._h, *([ptr] * 7), ptr, 1 << 40, None) == -2
+
+
 # ---------------------------------------------------------------- the main-attention schedule
 #
 # The kernels see the main part only through the planner's tile tables.  These
